@@ -1,0 +1,393 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 Q4_K SwiGLU FFN (one JSON line on rank 0).
+
+Workload: the LLaMA-7B-shaped decode FFN (hidden 4096, inter 11008, m = 1,
+seeded Q4_K weights, float32 activations). A step is one full call of the
+feed-forward block (all its kernels). The metric is weight bytes streamed per
+second (GB/s) against the measured HBM copy bandwidth; a secondary object
+reports the 27B-shaped long prefill (hidden 5120, inter 17408, m = 2048) in
+int8-equivalent TOPS against the measured dense fp16/bf16 tensor peak.
+
+Timing: W eager warm-up steps, then K steps replayed from a CUDA graph and
+timed with CUDA events on the capture stream, bracketed by a barrier and a
+device synchronisation on both sides. The weights rotate over enough replicas
+that more than three times the L2 size is touched between two uses of one
+replica, so every step streams its weights from HBM. nvidia-smi samples the
+SM clock and throttle reasons during the timed region.
+
+  python bench.py [--gpus N --steps K --warmup W]          this library
+  python bench.py --impl reference [...]                   the CPU oracle
+For N > 1 each rank runs an independent replica (the FFN does not shard here).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DECODE_CFG = 1
+PREFILL_CFG = 4
+L2_BYTES = 135_528_448
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-steps", type=int, default=30)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def src_hash(*files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "q4_swiglu_ffn_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str, sha: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if line.startswith("BENCH_TRAFFIC "):
+            d = json.loads(line[len("BENCH_TRAFFIC "):])
+            if d.get("src_sha") == sha:
+                return d.get("dram_bytes_per_launch")
+    return None
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", gpu_index], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples[-3:]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = sorted(float(p[1]) for p in win if p[1].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in win for n, v in zip(names, p[5:9]) if v.lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": float(win[0][2]),
+                "reasons": reasons, "samples": len(win)}
+
+
+# --------------------------------------------------------------------------- CPU baseline (oracle)
+def _cpu_decode_worker(budget_s: float, q):
+    import numpy as np
+    import oracle
+    import workloads
+    cfg = workloads.CONFIGS[DECODE_CFG]
+    wg, wu, wd = workloads.weights(cfg)
+    x, _ = workloads.activations(cfg)
+    reps, t_total = 0, 0.0
+    while t_total < budget_s and reps < 50:
+        t = time.perf_counter()
+        oracle.ffn_decode(x, wg, wu, wd)
+        t_total += time.perf_counter() - t
+        reps += 1
+    q.put({"reps": reps, "seconds": t_total, "bytes": cfg.weight_bytes() * reps})
+
+
+def cpu_baseline(budget_s: float):
+    """The oracle (numpy float64, unmodified) on the host cores, in a spawned process."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_cpu_decode_worker, args=(budget_s, q))
+    p.start()
+    r = q.get()
+    p.join()
+    cores = os.cpu_count()
+    return {"value": r["bytes"] / r["seconds"] / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{r['reps']} full LLaMA-7B-shaped decode FFN call(s) (m=1) of the numpy float64 oracle, "
+                      f"{r['seconds']:.1f} s; BLAS matvecs multi-threaded, per-block dequantisation "
+                      f"single-threaded"}
+
+
+# --------------------------------------------------------------------------- GPU side
+def gpu_decode(args, rank, world, dist):
+    import numpy as np
+    import torch
+    import workloads
+    import q4_swiglu_ffn_gb300 as q
+
+    cfg = workloads.CONFIGS[DECODE_CFG]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wbytes = cfg.weight_bytes()
+    R = max(2, math.ceil(3 * L2_BYTES / wbytes))
+    host = [workloads.weights(cfg), workloads.weights(cfg, seed=cfg.seed + 1000)]
+    reps = [tuple(torch.from_numpy(a).to(dev) for a in host[r % 2]) for r in range(R)]
+    x_np, _ = workloads.activations(cfg)
+    x = torch.from_numpy(x_np).to(dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+
+    def step(i):
+        wg, wu, wd = reps[i % R]
+        q.ffn_q4k_swiglu(x, wg, wu, wd, y=y)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    G = R * max(1, 64 // R)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    n_rep = max(1, math.ceil(args.steps / G))
+    K = n_rep * G
+
+    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index if world == 1 else 0]
+    sampler = ClockSampler(gpu_index.strip())
+    time.sleep(0.5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(n_rep):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist:
+        dist.barrier()
+    sampler.stop()
+    ms = e0.elapsed_time(e1)
+    clocks = sampler.summary(t0, t1)
+
+    # per-kernel durations (events around each kernel of the call; serialises them)
+    nk = 3
+    P = 300
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
+    for i in range(P):
+        q.q4k_set_profile_events(evs[i])
+        step(i)
+    q.q4k_set_profile_events(None)
+    torch.cuda.synchronize()
+    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(nk)]
+
+    # end to end: pinned host x in, host y out, every step
+    xh = torch.from_numpy(x_np).pin_memory()
+    yh = torch.empty(x_np.shape, dtype=torch.float32).pin_memory()
+    E = min(K, 2000)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(E):
+        x.copy_(xh, non_blocking=True)
+        step(i)
+        yh.copy_(y, non_blocking=True)
+        stream.synchronize()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    assert q.q4k_check_device_error() == 0
+    return {"ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "E": E, "R": R,
+            "wbytes": wbytes, "xbytes": x_np.nbytes}
+
+
+def gpu_prefill(args):
+    import torch
+    import workloads
+    import q4_swiglu_ffn_gb300 as q
+
+    cfg = workloads.CONFIGS[PREFILL_CFG]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wg, wu, wd = (torch.from_numpy(a).to(dev) for a in workloads.weights(cfg))
+    _, xb = workloads.activations(cfg)
+    import numpy as np
+    x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+    m, H, I = cfg.m, cfg.hidden, cfg.inter
+    ws = torch.zeros(q.ffn_q4k_workspace_bytes(m, H, I), dtype=torch.uint8, device=dev)
+    y = torch.empty((m, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        q.ffn_q4k_swiglu_ex(x, wg, wu, wd, ws, y=y)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.prefill_steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.prefill_steps
+    nk = 5
+    P = 10
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
+    for i in range(P):
+        q.q4k_set_profile_events(evs[i])
+        step()
+    q.q4k_set_profile_events(None)
+    torch.cuda.synchronize()
+    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(nk)]
+    assert q.q4k_check_device_error() == 0
+    return {"ms": ms, "kern_ms": kern_ms, "ops": cfg.int8_ops(), "cfg": cfg}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    import workloads
+    cfg = workloads.CONFIGS[DECODE_CFG]
+    metric = "Q4_K SwiGLU FFN: decode weight GB/s vs HBM peak; prefill int8 TOPS vs peak"
+    workload = {"workload": cfg.name, "hidden": cfg.hidden, "inter": cfg.inter, "m": cfg.m,
+                "weights": "seeded Q4_K (d, dmin ~ U[0.001, 0.05] fp16, 6-bit scales/mins, 4-bit quants uniform)",
+                "x": "float32 N(0,1)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = cpu_baseline(args.cpu_budget_s)
+        v = cb["value"]
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cfg.weight_bytes() / (v * 1e9) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload, "cpu_baseline": cb,
+                "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        dist = tdist
+    torch.cuda.set_device(local)
+    try:
+        import q4_swiglu_ffn_gb300  # noqa: F401
+    except ImportError:
+        import __graft_entry__
+        __graft_entry__.build()
+
+    r = gpu_decode(args, rank, world, dist)
+    ms = r["ms"]
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    units = r["wbytes"] * r["K"] * world
+    value = units / (ms * 1e-3) / 1e9
+    pk, pk_kind = peaks()
+
+    pre = None
+    if not args.no_prefill and rank == 0:
+        pre = gpu_prefill(args)
+    cb = cpu_baseline(args.cpu_budget_s) if (rank == 0 and world == 1) else None
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    # dominant kernel: gate+up GEMV (2/3 of the weight bytes)
+    k1_bytes = 2 * cfg.inter * (cfg.hidden // 256) * 144
+    k1_ms = r["kern_ms"][1]
+    ach = k1_bytes / (k1_ms * 1e-3) / 1e9
+    sha = src_hash("decode.cu", "common.cuh")
+    roof = {"kernel": "gemv_kernel<gate+up> (K1)", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth",
+            "traffic": profiled_traffic("decode_gateup_llama7b_m1.txt", sha),
+            "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_ms": k1_ms,
+            "step_frac": (r["wbytes"] / (ms / r["K"] * 1e-3) / 1e9) / pk["hbm_gbs"]}
+    e2e_val = r["wbytes"] * r["E"] / (r["e2e_ms"] * 1e-3) / 1e9
+    line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": r["K"],
+            "warmup": args.warmup, "ms_per_step": ms / r["K"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic",
+            "config": dict(workload, l2=f"rotating {r['R']} weight replicas ({r['R'] * r['wbytes'] / 1e6:.0f} MB "
+                                        f"> 3x the {L2_BYTES / 1e6:.0f} MB L2)", graph="CUDA graph replay",
+                           parallelism=f"replicas x{world}"),
+            "roofline": roof,
+            "kernels_ms": {"prep_x": r["kern_ms"][0], "gate_up_swiglu": r["kern_ms"][1], "down": r["kern_ms"][2]},
+            "cpu_baseline": cb,
+            "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": r["xbytes"],
+                    "d2h_bytes_per_step": r["xbytes"], "steps": r["E"],
+                    "note": "pinned host x -> device, the C-ABI call, device y -> pinned host, stream sync, every step"},
+            "gpu_launches": 3 * r["K"] * world,
+            "clocks": r["clocks"]}
+    if pre is not None:
+        c = pre["cfg"]
+        gu_ops = 2 * c.m * c.hidden * c.inter * 2
+        gu_ms = pre["kern_ms"][2]
+        peak_t = pk["bf16_tflops"]
+        line["prefill"] = {
+            "workload": c.name, "value": pre["ops"] / (pre["ms"] * 1e-3) / 1e12, "unit": "TOPS (int8-equivalent)",
+            "ms_per_step": pre["ms"],
+            "kernels_ms": dict(zip(["q8_1_x", "expand_x", "gate_up_mmq", "expand_h", "down_mmq"], pre["kern_ms"])),
+            "roofline": {"kernel": "mmq_kernel<gate+up> (tcgen05 kind::f16)", "bound": "tensor",
+                         "achieved": gu_ops / (gu_ms * 1e-3) / 1e12, "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": gu_ops / (gu_ms * 1e-3) / 1e12 / peak_t,
+                         "peak_kind": f"{pk_kind} dense bf16 (same tensor rate as fp16)",
+                         "note": "achieved counts the algorithmic int8-equivalent ops; the kernel executes 2x "
+                                 "that in fp16 (activations split into hi+lo)"},
+            "int8_mma_sync_peak_tops": 151.7}
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/*
+ * q4kffn.h -- C ABI of the GB300 (sm_103a) Q4_K SwiGLU feed-forward library.
+ *
+ * The library computes the LLaMA-style feed-forward block
+ *     y = W_down . ( silu(W_gate . x) * (W_up . x) )
+ * with weights stored as rows of GGML Q4_K blocks (256 weights in 144 bytes:
+ * fp16 d, fp16 dmin, 12 bytes of packed 6-bit scales and mins for 8
+ * sub-blocks of 32, 128 bytes of 4-bit quants).
+ *   Source: realizar src/cuda/executor/layers/ffn.rs, fused_ffn_swiglu_gpu
+ *   ("down(swiglu(gate(x), up(x)))", gate and up over the same input, all
+ *   launches chained on one stream with no synchronisation) and
+ *   fused_ffn_swiglu_gpu_true_dp4a (activations quantized to Q8_1 once for
+ *   gate and up, the activated vector re-quantized before down);
+ *   spark_model/layers/ops/q4k_mmq.rs (QK_K = 256, 144-byte blocks,
+ *   q4k_weight_bytes, quantize_act_q8_1, q4k_mmq_gemm, quantize_weight_q4k).
+ *
+ * Conventions for every entry point
+ *   - Pointers are DEVICE pointers owned by the caller unless a comment says
+ *     otherwise; the library never frees them. They must be 16-byte aligned.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned synchronously; nothing is written in that case.
+ *   - Faults inside kernels (a bounded device wait that ran out, a weight
+ *     block whose scale would overflow fp16) are recorded in a per-device
+ *     error word and returned by q4k_check_device_error().
+ *   - Shapes: hidden and inter (and every quantized dimension) must be
+ *     positive multiples of 256; m >= 1.
+ *   - Layouts: x and y are row-major [m][hidden]. W_gate and W_up hold `inter`
+ *     rows of hidden/256 blocks, W_down holds `hidden` rows of inter/256
+ *     blocks (row = output feature, blocks run along the input dimension;
+ *     realizar q4k_gemv_cached_uses.rs, q4k_gemv_cached: n = output, k = input).
+ *   - Regimes: m <= 8 runs the decode path (float32 activations, no
+ *     activation quantization); m >= 9 runs the prefill path (activations
+ *     quantized to Q8_1, Q4_K x Q8_1 GEMM on the tensor cores).
+ */
+#ifndef Q4KFFN_H
+#define Q4KFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  Q4K_OK = 0,
+  Q4K_ERR_NULL = 1,      /* a required pointer is NULL                                 */
+  Q4K_ERR_SHAPE = 2,     /* dim not a positive multiple of 256, m < 1, or size overflow */
+  Q4K_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned                           */
+  Q4K_ERR_DTYPE = 4,     /* unknown activation dtype                                   */
+  Q4K_ERR_CUDA = 5,      /* a CUDA runtime call or launch failed                       */
+  Q4K_ERR_ARCH = 6,      /* current device is not compute capability 10.3              */
+  Q4K_ERR_TIMEOUT = 7,   /* a bounded device wait ran out (reported after the fact)    */
+  Q4K_ERR_NOMEM = 8,     /* workspace allocation failed or caller workspace too small  */
+  Q4K_ERR_RANGE = 9      /* weight quantizer: a block scale does not fit in fp16       */
+} q4k_status;
+
+typedef enum { Q4K_F32 = 0, Q4K_BF16 = 1 } q4k_dtype;
+
+/* A cudaStream_t passed as an opaque handle. */
+typedef void* q4k_stream_t;
+
+/* Bytes of a Q4_K matrix of `rows` rows of `cols` inputs: rows*(cols/256)*144.
+ * Source: spark_model/layers/ops/q4k_mmq.rs, q4k_weight_bytes. Returns 0 for an
+ * invalid shape. */
+size_t q4k_weight_bytes(int64_t rows, int64_t cols);
+
+/* Bytes of a planar Q8_1 buffer for [m][k] activations: m*k int8 quants followed
+ * by m*(k/32) {float d, float s} pairs (d = block scale, s = d * sum of the 32
+ * quants). Returns 0 for an invalid shape. */
+size_t q8_1_bytes(int64_t m, int64_t k);
+
+/* Quantize float32 or bf16 weights [rows][cols] (row-major) to Q4_K blocks.
+ * Source: spark_model/layers/ops/q4k_mmq.rs, quantize_weight_q4k (load-time
+ * bf16 -> block_q4_K); the pages give no algorithm, so this is a deterministic
+ * min-max quantizer: per block, dmin is the smallest fp16 with 63*dmin covering
+ * the largest sub-block negative range, each 6-bit min the smallest integer
+ * covering its sub-block, d the smallest fp16 with 945*d covering the largest
+ * (max + dmin*min), each 6-bit scale the smallest integer covering its
+ * sub-block, and q = round((x + dmin*min)/(d*scale)) clamped to 0..15, all in
+ * float64 with one rounding per operation. Every value ends within half a
+ * quant step of its input. out_q4k: q4k_weight_bytes(rows, cols) bytes.
+ * A block whose scale would exceed 65504 sets Q4K_ERR_RANGE in the device
+ * error word (that block is written with zeros). */
+q4k_status q4k_quantize_weights(const void* W, q4k_dtype dtype, int64_t rows, int64_t cols,
+                                void* out_q4k, q4k_stream_t stream);
+
+/* Quantize float32 or bf16 activations [m][k] to planar Q8_1 (see q8_1_bytes).
+ * Source: realizar ffn.rs, fused_ffn_swiglu_gpu_true_dp4a ("per-block scale +
+ * 32 x int8"); spark_model q4k_mmq.rs, quantize_act_q8_1. Per block of 32, in
+ * float32 with one rounding per operation: d = amax/127, inv = 127/amax,
+ * q = round(x*inv) ties away from zero, s = d*sum(q); an all-zero block gives
+ * zeros. bf16 input is widened exactly. Output is bit-exact with that rule. */
+q4k_status q8_1_quantize_act(const void* x, q4k_dtype dtype, int64_t m, int64_t k,
+                             void* out_q8, q4k_stream_t stream);
+
+/* The feed-forward block with float32 activations x [m][hidden] and float32
+ * output y [m][hidden]. Uses a per-device workspace that the library grows on
+ * demand (cudaMalloc, guarded by a mutex, kept until process exit). The first
+ * call on a device also checks that it is an sm_103 part. Concurrent calls on
+ * different streams of one device must use ffn_q4k_swiglu_ex with separate
+ * workspaces. y must not alias x or the weights. */
+q4k_status ffn_q4k_swiglu(const void* x, int64_t m, int64_t hidden, int64_t inter,
+                          const void* W_gate, const void* W_up, const void* W_down,
+                          float* y, q4k_stream_t stream);
+
+/* As ffn_q4k_swiglu, with an explicit activation dtype (Q4K_F32 or Q4K_BF16)
+ * and a caller-owned device workspace of at least
+ * ffn_q4k_workspace_bytes(m, hidden, inter) bytes, 256-byte aligned. Its
+ * contents need no initialisation (every call sets up what it reads). Calls
+ * sharing one workspace must not overlap on the GPU. */
+q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden,
+                             int64_t inter, const void* W_gate, const void* W_up,
+                             const void* W_down, float* y, void* workspace, size_t ws_bytes,
+                             q4k_stream_t stream);
+
+/* Workspace bytes ffn_q4k_swiglu_ex needs for this shape (0 for an invalid shape). */
+size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
+
+/* Byte offset and size, inside an ffn_q4k_swiglu_ex workspace, of the planar
+ * Q8_1 copy of the activated vector h = silu(gate)*up that the prefill path
+ * feeds to the down projection (m >= 9 only; test hook, offset 0 / size 0 for
+ * decode shapes). */
+size_t ffn_q4k_workspace_h_q8_1_offset(int64_t m, int64_t hidden, int64_t inter);
+
+/* Test hook: dequantize a Q4_K matrix to float32 [rows][cols]. Every value is
+ * d*scale*q - dmin*min rounded once to float32 (bit-exact). */
+q4k_status q4k_dequantize(const void* q4k, int64_t rows, int64_t cols, float* out,
+                          q4k_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device. Returns Q4K_OK, Q4K_ERR_TIMEOUT, Q4K_ERR_RANGE or
+ * Q4K_ERR_CUDA (a sticky runtime error). */
+q4k_status q4k_check_device_error(q4k_stream_t stream);
+
+/* Per-kernel timing hook (for benchmarks). After this call, every FFN call made
+ * on this thread records events[2i] (cudaEvent_t) before and events[2i+1] after
+ * its i-th kernel, for i < n/2, on the call's stream. Decode calls launch 3
+ * kernels (activation fragments, gate+up+SwiGLU, down), prefill calls 5 (Q8_1
+ * of x, operand expansion, gate+up MMQ + SwiGLU + Q8_1 of h, operand expansion,
+ * down MMQ). The events stay owned by the caller; n = 0 (events NULL) turns the
+ * hook off. Recording between kernels serialises them, so timed runs of the
+ * whole call leave the hook off. */
+q4k_status q4k_set_profile_events(void* const* events, int n);
+
+/* Status of the most recent failed host-side call on this thread (Q4K_OK if none). */
+q4k_status q4k_get_last_error(void);
+
+/* Static, human-readable name of a status. */
+const char* q4k_status_string(q4k_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4KFFN_H */

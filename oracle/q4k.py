@@ -128,7 +128,8 @@ def quantize_q8_1(x: np.ndarray):
     operation (the reading of "round-to-nearest of x*127/absmax"):
       amax = max|x|; d = amax/127; inv = 127/amax; q = round(x*inv) with ties
       away from zero, clamped to [-127, 127]; s = d * sum(q).
-    An all-zero block gives d = s = 0 and q = 0.
+    A block whose amax is below 2**-120 (zero, or so small that 127/amax would
+    overflow float32) gives d = s = 0 and q = 0.
     Returns (q int8 [m, k], d float32 [m, k/32], s float32 [m, k/32]).
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -136,8 +137,8 @@ def quantize_q8_1(x: np.ndarray):
     assert k % Q8_BLOCK == 0
     xb = x.reshape(m, k // Q8_BLOCK, Q8_BLOCK)
     amax = np.max(np.abs(xb), axis=-1)
-    nz = amax > 0
-    with np.errstate(divide="ignore", invalid="ignore"):
+    nz = amax >= np.float32(2.0 ** -120)
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
         d = np.where(nz, amax / np.float32(127.0), np.float32(0.0)).astype(np.float32)
         inv = np.where(nz, np.float32(127.0) / amax, np.float32(0.0)).astype(np.float32)
     v = (xb * inv[..., None]).astype(np.float32)

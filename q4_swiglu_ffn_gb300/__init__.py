@@ -1,0 +1,172 @@
+"""Python binding of libq4kffn.so, the sm_103a Q4_K SwiGLU feed-forward library.
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels. Tensors are torch CUDA tensors (PyTorch supplies device memory and
+streams); the functions take the same names and argument order as the C ABI
+in include/q4kffn.h. Importing this module raises if the library has not
+been built (``python q4_swiglu_ffn_gb300/build.py``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libq4kffn.so")
+
+Q4K_F32, Q4K_BF16 = 0, 1
+STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN", 4: "Q4K_ERR_DTYPE",
+          5: "Q4K_ERR_CUDA", 6: "Q4K_ERR_ARCH", 7: "Q4K_ERR_TIMEOUT", 8: "Q4K_ERR_NOMEM", 9: "Q4K_ERR_RANGE"}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python q4_swiglu_ffn_gb300/build.py`")
+
+lib = ctypes.CDLL(LIB_PATH)
+PREFILL_READY = True
+
+_i64, _sz, _p, _int = ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_int
+_SIGS = {
+    "q4k_weight_bytes": (_sz, [_i64, _i64]),
+    "q8_1_bytes": (_sz, [_i64, _i64]),
+    "q4k_quantize_weights": (_int, [_p, _int, _i64, _i64, _p, _p]),
+    "q8_1_quantize_act": (_int, [_p, _int, _i64, _i64, _p, _p]),
+    "ffn_q4k_swiglu": (_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
+    "ffn_q4k_swiglu_ex": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
+    "ffn_q4k_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "ffn_q4k_workspace_h_q8_1_offset": (_sz, [_i64, _i64, _i64]),
+    "q4k_dequantize": (_int, [_p, _i64, _i64, _p, _p]),
+    "q4k_check_device_error": (_int, [_p]),
+    "q4k_set_profile_events": (_int, [_p, _int]),
+    "q4k_get_last_error": (_int, []),
+    "q4k_status_string": (ctypes.c_char_p, [_int]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class Q4KError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({lib.q4k_status_string(status).decode()})")
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise Q4KError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return Q4K_F32
+    if t.dtype == torch.bfloat16:
+        return Q4K_BF16
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def q4k_weight_bytes(rows: int, cols: int) -> int:
+    return lib.q4k_weight_bytes(rows, cols)
+
+
+def q8_1_bytes(m: int, k: int) -> int:
+    return lib.q8_1_bytes(m, k)
+
+
+def ffn_q4k_workspace_bytes(m: int, hidden: int, inter: int) -> int:
+    return lib.ffn_q4k_workspace_bytes(m, hidden, inter)
+
+
+def ffn_q4k_workspace_h_q8_1_offset(m: int, hidden: int, inter: int) -> int:
+    return lib.ffn_q4k_workspace_h_q8_1_offset(m, hidden, inter)
+
+
+def q4k_quantize_weights(W, out=None, stream=None):
+    """W: [rows, cols] float32/bf16 CUDA tensor -> uint8 Q4_K blocks [rows, cols/256, 144]."""
+    import torch
+    rows, cols = W.shape
+    if out is None:
+        out = torch.empty((rows, cols // 256, 144), dtype=torch.uint8, device=W.device)
+    _check(lib.q4k_quantize_weights(_ptr(W), _dtype_code(W), rows, cols, _ptr(out), _stream(stream)),
+           "q4k_quantize_weights")
+    return out
+
+
+def q8_1_quantize_act(x, out=None, stream=None):
+    """x: [m, k] float32/bf16 CUDA tensor -> planar Q8_1 bytes (uint8, q8_1_bytes(m, k))."""
+    import torch
+    m, k = x.shape
+    if out is None:
+        out = torch.empty(q8_1_bytes(m, k), dtype=torch.uint8, device=x.device)
+    _check(lib.q8_1_quantize_act(_ptr(x), _dtype_code(x), m, k, _ptr(out), _stream(stream)), "q8_1_quantize_act")
+    return out
+
+
+def ffn_q4k_swiglu(x, W_gate, W_up, W_down, y=None, stream=None):
+    """y = W_down (silu(W_gate x) * (W_up x)); x float32 [m, hidden] -> y float32 [m, hidden]."""
+    import torch
+    m, hidden = x.shape
+    inter = W_gate.shape[0]
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    _check(lib.ffn_q4k_swiglu(_ptr(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(y),
+                              _stream(stream)), "ffn_q4k_swiglu")
+    return y
+
+
+def ffn_q4k_swiglu_ex(x, W_gate, W_up, W_down, workspace, y=None, stream=None):
+    """As ffn_q4k_swiglu with float32 or bf16 x and a caller workspace (uint8 CUDA tensor, zeroed once)."""
+    import torch
+    m, hidden = x.shape
+    inter = W_gate.shape[0]
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    _check(lib.ffn_q4k_swiglu_ex(_ptr(x), _dtype_code(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up),
+                                 _ptr(W_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "ffn_q4k_swiglu_ex")
+    return y
+
+
+def q4k_dequantize(q, rows: int, cols: int, out=None, stream=None):
+    """Test hook: Q4_K blocks -> float32 [rows, cols]."""
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=q.device)
+    _check(lib.q4k_dequantize(_ptr(q), rows, cols, _ptr(out), _stream(stream)), "q4k_dequantize")
+    return out
+
+
+def q4k_check_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status code."""
+    return lib.q4k_check_device_error(_stream(stream))
+
+
+def q4k_set_profile_events(events) -> None:
+    """Record torch.cuda.Event pairs around each kernel of the following FFN calls (None: off)."""
+    global _prof_keep
+    if not events:
+        _check(lib.q4k_set_profile_events(None, 0), "q4k_set_profile_events")
+        _prof_keep = None
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _prof_keep = arr  # the library keeps the pointer; keep the array alive
+    _check(lib.q4k_set_profile_events(arr, len(events)), "q4k_set_profile_events")
+
+
+_prof_keep = None
+
+
+def q4k_get_last_error() -> int:
+    return lib.q4k_get_last_error()

@@ -1,0 +1,251 @@
+// C ABI of the Q4_K SwiGLU FFN library: argument validation, per-device state
+// (architecture check, error word, default workspace) and dispatch by regime.
+// Conventions (see include/q4kffn.h): device pointers owned by the caller,
+// work enqueued on the caller's stream without synchronisation, argument
+// errors returned before anything is launched (realizar
+// q4k_gemv_cached_uses.rs, q4k_gemv_indexed_async: refuse a null weight
+// pointer before launch; libmir micro_moe.rs: checked size arithmetic).
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "q4kffn.h"
+
+namespace {
+
+thread_local q4k_status g_last = Q4K_OK;
+thread_local q4k::ProfileEvents g_prof;
+
+q4k_status fail(q4k_status s) {
+  g_last = s;
+  return s;
+}
+
+constexpr int MAX_DEV = 64;
+constexpr int64_t MAX_DIM = int64_t(1) << 20;   // rows, columns and tokens
+constexpr int64_t MAX_ELEMS = int64_t(1) << 36; // elements of one operand
+
+struct DeviceState {
+  bool checked = false;
+  bool ok = false;
+  int sms = 0;
+  uint32_t* err = nullptr;  // device error word
+  void* ws = nullptr;       // default workspace of ffn_q4k_swiglu
+  size_t ws_bytes = 0;
+  std::mutex mu;
+};
+std::mutex g_mu;
+DeviceState g_dev[MAX_DEV];
+
+q4k_status device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) return Q4K_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.checked) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return Q4K_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3);
+    if (d.ok) {
+      if (cudaMalloc(&d.err, sizeof(uint32_t)) != cudaSuccess) return Q4K_ERR_NOMEM;
+      if (cudaMemset(d.err, 0, sizeof(uint32_t)) != cudaSuccess) return Q4K_ERR_CUDA;
+    }
+    d.checked = true;
+  }
+  if (!d.ok) return Q4K_ERR_ARCH;
+  *out = &d;
+  return Q4K_OK;
+}
+
+bool dim_ok(int64_t v) { return v > 0 && v <= MAX_DIM && v % q4k::QK == 0; }
+bool tokens_ok(int64_t m) { return m >= 1 && m <= MAX_DIM; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+q4k_status check_ffn_args(const void* x, int dtype, int64_t m, int64_t hidden, int64_t inter, const void* wg,
+                          const void* wu, const void* wd, const float* y) {
+  if (!x || !wg || !wu || !wd || !y) return Q4K_ERR_NULL;
+  if (dtype != Q4K_F32 && dtype != Q4K_BF16) return Q4K_ERR_DTYPE;
+  if (!tokens_ok(m) || !dim_ok(hidden) || !dim_ok(inter)) return Q4K_ERR_SHAPE;
+  if (m * hidden > MAX_ELEMS || m * inter > MAX_ELEMS || hidden * inter > MAX_ELEMS) return Q4K_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(wg) || !aligned16(wu) || !aligned16(wd) || !aligned16(y)) return Q4K_ERR_ALIGN;
+  return Q4K_OK;
+}
+
+bool is_decode(int64_t m) { return m <= 8; }
+
+size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
+  if (is_decode(m)) {
+    q4k::DecodePlan p;
+    return q4k::decode_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
+  }
+  q4k::PrefillPlan p;
+  return q4k::prefill_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
+}
+
+q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t inter, const void* wg,
+                   const void* wu, const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+  cudaError_t e;
+  if (is_decode(m)) {
+    q4k::DecodePlan p;
+    if (!q4k::decode_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
+    e = q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof);
+  } else {
+    q4k::PrefillPlan p;
+    if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
+    e = q4k::launch_prefill(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof);
+  }
+  return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t q4k_weight_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || rows > MAX_DIM || !dim_ok(cols)) return 0;
+  return (size_t)rows * (size_t)(cols / q4k::QK) * q4k::BLK;
+}
+
+size_t q8_1_bytes(int64_t m, int64_t k) {
+  if (!tokens_ok(m) || !dim_ok(k)) return 0;
+  return (size_t)m * (size_t)k + (size_t)m * (size_t)(k / q4k::Q8B) * 8;
+}
+
+q4k_status q4k_quantize_weights(const void* W, q4k_dtype dtype, int64_t rows, int64_t cols, void* out_q4k,
+                                q4k_stream_t stream) {
+  if (!W || !out_q4k) return fail(Q4K_ERR_NULL);
+  if (dtype != Q4K_F32 && dtype != Q4K_BF16) return fail(Q4K_ERR_DTYPE);
+  if (rows <= 0 || rows > MAX_DIM || !dim_ok(cols) || rows * cols > MAX_ELEMS) return fail(Q4K_ERR_SHAPE);
+  if (!aligned16(W) || !aligned16(out_q4k)) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  if (q4k::launch_quantize_weights(W, dtype == Q4K_BF16, rows, cols, out_q4k, d->err, (cudaStream_t)stream) !=
+      cudaSuccess)
+    return fail(Q4K_ERR_CUDA);
+  return Q4K_OK;
+}
+
+q4k_status q8_1_quantize_act(const void* x, q4k_dtype dtype, int64_t m, int64_t k, void* out_q8,
+                             q4k_stream_t stream) {
+  if (!x || !out_q8) return fail(Q4K_ERR_NULL);
+  if (dtype != Q4K_F32 && dtype != Q4K_BF16) return fail(Q4K_ERR_DTYPE);
+  if (!tokens_ok(m) || !dim_ok(k) || m * k > MAX_ELEMS) return fail(Q4K_ERR_SHAPE);
+  if (!aligned16(x) || !aligned16(out_q8)) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  if (q4k::launch_q8_1(x, dtype == Q4K_BF16, m, k, out_q8, (cudaStream_t)stream) != cudaSuccess)
+    return fail(Q4K_ERR_CUDA);
+  return Q4K_OK;
+}
+
+q4k_status ffn_q4k_swiglu(const void* x, int64_t m, int64_t hidden, int64_t inter, const void* W_gate,
+                          const void* W_up, const void* W_down, float* y, q4k_stream_t stream) {
+  q4k_status st = check_ffn_args(x, Q4K_F32, m, hidden, inter, W_gate, W_up, W_down, y);
+  if (st != Q4K_OK) return fail(st);
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  std::lock_guard<std::mutex> lk(d->mu);
+  const size_t need = plan_bytes(m, hidden, inter, d->sms);
+  if (need == 0) return fail(Q4K_ERR_SHAPE);
+  if (d->ws_bytes < need) {
+    if (d->ws) cudaFree(d->ws);  // synchronises the device, so no call still uses it
+    d->ws = nullptr;
+    d->ws_bytes = 0;
+    if (cudaMalloc(&d->ws, need) != cudaSuccess) return fail(Q4K_ERR_NOMEM);
+    if (cudaMemset(d->ws, 0, need) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+    d->ws_bytes = need;
+  }
+  st = run_ffn(x, Q4K_F32, m, hidden, inter, W_gate, W_up, W_down, y, d->ws, d, (cudaStream_t)stream);
+  return st == Q4K_OK ? st : fail(st);
+}
+
+q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden, int64_t inter,
+                             const void* W_gate, const void* W_up, const void* W_down, float* y, void* workspace,
+                             size_t ws_bytes, q4k_stream_t stream) {
+  q4k_status st = check_ffn_args(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y);
+  if (st != Q4K_OK) return fail(st);
+  if (!workspace) return fail(Q4K_ERR_NULL);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  const size_t need = plan_bytes(m, hidden, inter, d->sms);
+  if (need == 0) return fail(Q4K_ERR_SHAPE);
+  if (ws_bytes < need) return fail(Q4K_ERR_NOMEM);
+  st = run_ffn(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
+  return st == Q4K_OK ? st : fail(st);
+}
+
+size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {
+  if (!tokens_ok(m) || !dim_ok(hidden) || !dim_ok(inter)) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != Q4K_OK) return 0;
+  return plan_bytes(m, hidden, inter, d->sms);
+}
+
+size_t ffn_q4k_workspace_h_q8_1_offset(int64_t m, int64_t hidden, int64_t inter) {
+  if (!tokens_ok(m) || !dim_ok(hidden) || !dim_ok(inter) || is_decode(m)) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != Q4K_OK) return 0;
+  q4k::PrefillPlan p;
+  return q4k::prefill_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
+}
+
+q4k_status q4k_dequantize(const void* q4k_, int64_t rows, int64_t cols, float* out, q4k_stream_t stream) {
+  if (!q4k_ || !out) return fail(Q4K_ERR_NULL);
+  if (rows <= 0 || rows > MAX_DIM || !dim_ok(cols) || rows * cols > MAX_ELEMS) return fail(Q4K_ERR_SHAPE);
+  if (!aligned16(q4k_) || !aligned16(out)) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  if (q4k::launch_dequant(q4k_, out, rows, cols, (cudaStream_t)stream) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+  return Q4K_OK;
+}
+
+q4k_status q4k_check_device_error(q4k_stream_t stream) {
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, d->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+  if (word && cudaMemset(d->err, 0, sizeof(word)) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+  if (word & q4k::ERRBIT_TIMEOUT) return fail(Q4K_ERR_TIMEOUT);
+  if (word & q4k::ERRBIT_RANGE) return fail(Q4K_ERR_RANGE);
+  return Q4K_OK;
+}
+
+q4k_status q4k_set_profile_events(void* const* events, int n) {
+  if (n < 0 || (n > 0 && !events)) return fail(Q4K_ERR_NULL);
+  g_prof.ev = n > 0 ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events)) : nullptr;
+  g_prof.n = n;
+  return Q4K_OK;
+}
+
+q4k_status q4k_get_last_error(void) { return g_last; }
+
+const char* q4k_status_string(q4k_status s) {
+  switch (s) {
+    case Q4K_OK: return "ok";
+    case Q4K_ERR_NULL: return "null pointer";
+    case Q4K_ERR_SHAPE: return "invalid shape";
+    case Q4K_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case Q4K_ERR_DTYPE: return "unsupported dtype";
+    case Q4K_ERR_CUDA: return "CUDA error";
+    case Q4K_ERR_ARCH: return "device is not sm_103";
+    case Q4K_ERR_TIMEOUT: return "bounded device wait timed out";
+    case Q4K_ERR_NOMEM: return "workspace allocation failed or too small";
+    case Q4K_ERR_RANGE: return "quantized scale outside the fp16 range";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,569 @@
+// Decode regime (m = 1..8 tokens) of the Q4_K SwiGLU FFN on sm_103a.
+//
+//   K0 prep_x:       x [m][hidden] fp32 -> B fragments (below)
+//   K1 gemv<2>:      g = Wg.x, u = Wu.x in one pass over both weight rows,
+//                    h = silu(g) * u, then h -> B fragments for K2
+//   K2 gemv<1>:      y = Wd.h
+// K1 and K2 are launched with programmatic dependent launch, so each starts
+// streaming its weights while the previous kernel drains.
+// Source: realizar src/cuda/executor/layers/ffn.rs, fused_ffn_swiglu_gpu
+// (gate and up GEMVs of the same input, fused SwiGLU, down GEMV, chained on
+// one stream without synchronisation); realizar q4k_gemv_cached_uses.rs,
+// TiledQ4KGemv / ChunkedTiledQ4KGemv (activations staged once and reused by
+// several output rows; K chunked when it is large) as prior art.
+//
+// Arithmetic. The weights are multiplied on the tensor cores with
+// mma.sync.m16n8k16 (fp16 inputs, fp32 accumulation). A weight tile (16 rows
+// x 16 k) is the A operand: each 4-bit quant q is widened with the
+// 0x6400-exponent trick and multiplied by its 6-bit sub-block scale in one
+// fp16 fma, giving q*scale exactly (<= 945). The activations are the B
+// operand: column n = (token 4*tile + n/2, part n%2), part 0 the fp16 value of
+// x*2^-e and part 1 the fp16 remainder, so hi + lo carries about 22 bits of x.
+// e is chosen per token and superblock so that the largest |x| maps into
+// [2^14, 2^15). Per superblock the MMA result is scaled by d * 2^e and the
+// min term dmin * sum_j min_j * X_j (X_j = sum of x over sub-block j) is
+// subtracted; that term comes from one extra MMA whose A holds the 6-bit
+// mins and whose B holds X_j * 2^-(e+6) split into hi and lo.
+//
+// Work split. Each warp streams its own weight rows through a ring of shared
+// memory stages filled by 144-byte bulk copies (one per row per superblock),
+// so every warp keeps several KB of weights in flight without using
+// registers. A unit of work is (K-split, 16-row tile); each CTA takes a
+// contiguous range of units and its warps take units round-robin. When K is
+// split, partial sums go to the workspace and the last warp to finish a tile
+// (per-tile semaphore) adds them in a fixed order, so results are
+// deterministic. The last warp to finish the 16 tiles of a 256-row block of h
+// converts that block to B fragments for K2.
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q4k {
+
+namespace {
+
+struct FragPtrs {
+  uint2* fx;     // [nsb][16 k-steps][nt][32 lanes] main B fragments
+  uint32_t* fm;  // [nsb][nt][32 lanes] min-term B fragments (b0b1; b2b3 are zero)
+  float* sc;     // [nsb][8] 2^e per token
+};
+
+// Loads the 8 inputs of this lane for one token (float32 or bf16, widened exactly).
+__device__ __forceinline__ void load_inputs8(const float* p, bool coherent, float v[8]) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+  const float4 a = coherent ? __ldcg(q) : q[0];
+  const float4 b = coherent ? __ldcg(q + 1) : q[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load_inputs8(const __nv_bfloat16* p, bool, float v[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// One warp converts superblock `sb` (256 consecutive inputs) of m rows of src
+// (row stride ld elements) into B fragments. Tokens m..4*nt-1 get zeros.
+template <typename T>
+__device__ void prep_superblock(const T* src, int64_t ld, int m, int nt, int sb, FragPtrs f, bool coherent) {
+  const int lane = threadIdx.x & 31;
+  const int sbk = lane >> 2;              // sub-block of this lane's 8 inputs
+  const int tgp = sbk >> 1, p = sbk & 1;  // quad thread owning that sub-block and its nibble half
+  for (int t = 0; t < 4 * nt; ++t) {
+    float v[8];
+    if (t < m) {
+      load_inputs8(src + (int64_t)t * ld + (int64_t)sb * QK + lane * 8, coherent, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = warp_max(amax);
+    int e = 0;
+    if (amax > 0.f) e = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100);
+    const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+    __half hi[8], lo[8];
+    float xsum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = v[i] * s;
+      hi[i] = __float2half_rn(y);
+      lo[i] = __float2half_rn(y - __half2float(hi[i]));
+      xsum += y;
+    }
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+    xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+    const int ntile = t >> 2, gbase = 2 * (t & 3);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int w = (lane & 3) * 2 + hh;
+      const int step = 2 * w + p;
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const __half* h8 = part ? lo : hi;
+        uint2 fr;
+        fr.x = h2_as_u32(__halves2half2(h8[4 * hh + 0], h8[4 * hh + 2]));
+        fr.y = h2_as_u32(__halves2half2(h8[4 * hh + 1], h8[4 * hh + 3]));
+        f.fx[(((int64_t)sb * 16 + step) * nt + ntile) * 32 + (gbase + part) * 4 + tgp] = fr;
+      }
+    }
+    // X_j * 2^-6 keeps the sub-block sums inside the fp16 range
+    const float xl = __shfl_sync(0xffffffffu, xsum, lane & ~7) * 0.015625f;
+    const float xh = __shfl_sync(0xffffffffu, xsum, (lane & ~7) + 4) * 0.015625f;
+    if ((lane & 7) == 0) {
+      const __half xlh = __float2half_rn(xl), xhh = __float2half_rn(xh);
+      const __half xll = __float2half_rn(xl - __half2float(xlh)), xhl = __float2half_rn(xh - __half2float(xhh));
+      const int tq = lane >> 3;
+      f.fm[((int64_t)sb * nt + ntile) * 32 + (gbase + 0) * 4 + tq] = h2_as_u32(__halves2half2(xlh, xhh));
+      f.fm[((int64_t)sb * nt + ntile) * 32 + (gbase + 1) * 4 + tq] = h2_as_u32(__halves2half2(xll, xhl));
+    }
+    if (lane == 0) f.sc[(int64_t)sb * 8 + t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  }
+}
+
+// K0 also zeroes the split-K semaphores and h-block counters of this call; K1
+// and K2 touch them only after their dependent-launch wait on K0.
+template <typename T>
+__global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f,
+                              uint32_t* __restrict__ counters, int ncounters) {
+  pdl_launch_dependents();
+  for (int i = blockIdx.x * 32 + threadIdx.x; i < ncounters; i += gridDim.x * 32) counters[i] = 0u;
+  prep_superblock<T>(x, hidden, m, nt, blockIdx.x, f, false);
+}
+
+struct GemvParams {
+  const uint8_t* w0;  // gate (K1) or down (K2)
+  const uint8_t* w1;  // up (K1)
+  int rows, nsb, m, kc, nks;
+  FragPtrs in;        // B fragments of the input
+  float* part;        // [nks][nmat][m][rows] partial sums when nks > 1
+  uint32_t* sem;      // [rows/16] per-tile semaphores (zero between calls)
+  float* out;         // h (K1) or y (K2), [m][rows]
+  FragPtrs next;      // K1: fragments of h for K2
+  uint32_t* cnt_next; // K1: [rows/256] counters (zero between calls)
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+template <int NMAT, int NT, int STAGES, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P) {
+  constexpr int ROWS = 16;
+  constexpr int STAGE_BYTES = NMAT * ROWS * BLK;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  uint8_t* ring = smem + warp * STAGES * STAGE_BYTES;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * STAGE_BYTES) + warp * STAGES;
+
+  const int nrt = P.rows / ROWS;
+  const int64_t U = (int64_t)P.nks * nrt;
+  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // issue cursor (which step the next bulk copy loads)
+  int64_t iu = u0 + warp;
+  int isb = 0, isb_end = 0, irt = 0;
+  if (iu < u1) {
+    irt = (int)(iu % nrt);
+    isb = (int)(iu / nrt) * P.kc;
+    isb_end = min(P.nsb, isb + P.kc);
+  }
+  const uint64_t pol = policy_evict_first();
+  auto issue = [&](int stage) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    uint8_t* dst = ring + stage * STAGE_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(&bar[stage], STAGE_BYTES);
+    __syncwarp();
+    if (lane < NMAT * ROWS) {
+      const int mat = lane / ROWS, r = lane % ROWS;
+      const uint8_t* src = (mat ? P.w1 : P.w0) + ((int64_t)(irt * ROWS + r) * P.nsb + isb) * BLK;
+      bulk_g2s_hint(dst + lane * BLK, src, BLK, &bar[stage], pol);
+    }
+    if (++isb == isb_end) {
+      iu += WARPS;
+      if (iu < u1) {
+        irt = (int)(iu % nrt);
+        isb = (int)(iu / nrt) * P.kc;
+        isb_end = min(P.nsb, isb + P.kc);
+      }
+    }
+  };
+
+  int issued = 0;
+  for (; issued < STAGES - 1 && iu < u1; ++issued) issue(issued % STAGES);
+  pdl_launch_dependents();
+  pdl_wait();  // input fragments come from the previous kernel
+
+  // consume cursor
+  int64_t cu = u0 + warp;
+  int csb = 0, csb_end = 0, crt = 0, cks = 0;
+  if (cu < u1) {
+    crt = (int)(cu % nrt);
+    cks = (int)(cu / nrt);
+    csb = cks * P.kc;
+    csb_end = min(P.nsb, csb + P.kc);
+  }
+  float acc[NMAT][NT][2];
+#pragma unroll
+  for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[a][n][0] = acc[a][n][1] = 0.f;
+
+  int step = 0;
+  bool failed = false;
+  while (cu < u1) {
+    const int stage = step % STAGES;
+    if (iu < u1) {
+      issue((step + STAGES - 1) % STAGES);
+      ++issued;
+    }
+    if (!mbar_wait(&bar[stage], (uint32_t)(step / STAGES) & 1u, P.err)) {
+      failed = true;
+      break;
+    }
+    // ------------------------------------------------ one superblock of 16 rows
+    const uint8_t* st = ring + stage * STAGE_BYTES;
+    uint4 q0[NMAT][2], q1[NMAT][2];
+    uint32_t A_min[NMAT][2];
+    __half2 mlo[NMAT][2], alo[NMAT][2], mhi[NMAT][2], ahi[NMAT][2];
+    float dd[NMAT][2], dm[NMAT][2];
+#pragma unroll
+    for (int a = 0; a < NMAT; ++a) {
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint8_t* rb = st + (a * ROWS + g + 8 * r) * BLK;
+        const uint4 hd = *reinterpret_cast<const uint4*>(rb);
+        q0[a][r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
+        q1[a][r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
+        dd[a][r] = fp16_bits_to_f32(hd.x);
+        dm[a][r] = fp16_bits_to_f32(hd.x >> 16);
+        uint32_t sl, ml, sh, mh;
+        scale_min(hd.y, hd.z, hd.w, 2 * tig, sl, ml);
+        scale_min(hd.y, hd.z, hd.w, 2 * tig + 1, sh, mh);
+        mlo[a][r] = __float2half2_rn((float)sl);
+        alo[a][r] = __float2half2_rn(-1024.f * (float)sl);
+        mhi[a][r] = __float2half2_rn((float)sh * 0.0625f);
+        ahi[a][r] = __float2half2_rn(-64.f * (float)sh);
+        A_min[a][r] = h2_as_u32(__halves2half2(__uint2half_rn(ml), __uint2half_rn(mh)));
+      }
+    }
+    float c[NMAT][NT][4], cm[NMAT][NT][4];
+#pragma unroll
+    for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c[a][n][i] = cm[a][n][i] = 0.f;
+
+    const uint2* fx = P.in.fx + (int64_t)csb * 16 * NT * 32 + lane;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      uint2 b0[NT], b1[NT];
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        b0[n] = fx[((2 * w) * NT + n) * 32];
+        b1[n] = fx[((2 * w + 1) * NT + n) * 32];
+      }
+#pragma unroll
+      for (int a = 0; a < NMAT; ++a) {
+        uint32_t L0[2], L1[2], H0[2], H1[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint4& qq = (w < 4) ? q0[a][r] : q1[a][r];
+          const uint32_t wd = (w & 3) == 0 ? qq.x : (w & 3) == 1 ? qq.y : (w & 3) == 2 ? qq.z : qq.w;
+          const uint32_t t8 = wd >> 8;
+          L0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x000F000Fu, 0x64006400u)), mlo[a][r], alo[a][r]));
+          L1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x000F000Fu, 0x64006400u)), mlo[a][r], alo[a][r]));
+          H0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x00F000F0u, 0x64006400u)), mhi[a][r], ahi[a][r]));
+          H1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x00F000F0u, 0x64006400u)), mhi[a][r], ahi[a][r]));
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          mma16816(c[a][n], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
+          mma16816(c[a][n], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
+        }
+      }
+    }
+    {
+      const uint32_t* fm = P.in.fm + (int64_t)csb * NT * 32 + lane;
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        const uint32_t bm = fm[n * 32];
+#pragma unroll
+        for (int a = 0; a < NMAT; ++a) mma16816(cm[a][n], A_min[a][0], A_min[a][1], 0u, 0u, bm, 0u);
+      }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      const float xs = P.in.sc[(int64_t)csb * 8 + n * 4 + tig];
+#pragma unroll
+      for (int a = 0; a < NMAT; ++a) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const float main = c[a][n][2 * r] + c[a][n][2 * r + 1];
+          const float mins = cm[a][n][2 * r] + cm[a][n][2 * r + 1];
+          acc[a][n][r] = fmaf(main, dd[a][r] * xs, acc[a][n][r]);
+          acc[a][n][r] = fmaf(-mins, dm[a][r] * (64.f * xs), acc[a][n][r]);
+        }
+      }
+    }
+    ++step;
+    // ------------------------------------------------ end of a unit
+    if (++csb == csb_end) {
+      const int row0 = crt * ROWS;
+      bool last = true;
+      if (P.nks > 1) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int tok = n * 4 + tig;
+          if (tok < P.m) {
+#pragma unroll
+            for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+              for (int r = 0; r < 2; ++r)
+                P.part[(((int64_t)cks * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r] = acc[a][n][r];
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        uint32_t old = 0;
+        if (lane == 0) old = atomicAdd(&P.sem[crt], 1u);
+        old = __shfl_sync(0xffffffffu, old, 0);
+        last = (old == (uint32_t)(P.nks - 1));
+        if (last) {
+          __threadfence();
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const int tok = n * 4 + tig;
+            if (tok < P.m) {
+#pragma unroll
+              for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  float s = 0.f;
+                  for (int k = 0; k < P.nks; ++k)
+                    s += __ldcg(&P.part[(((int64_t)k * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r]);
+                  acc[a][n][r] = s;
+                }
+            }
+          }
+          if (lane == 0) P.sem[crt] = 0u;
+        }
+      }
+      if (last) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          const int tok = n * 4 + tig;
+          if (tok < P.m) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const float v = (NMAT == 2) ? silu_f(acc[0][n][r]) * acc[NMAT - 1][n][r] : acc[0][n][r];
+              P.out[(int64_t)tok * P.rows + row0 + g + 8 * r] = v;
+            }
+          }
+        }
+        if (NMAT == 2) {
+          // the last of the 16 tiles of a 256-row block of h converts it for the down projection
+          __threadfence();
+          __syncwarp();
+          const int sbh = row0 / QK;
+          uint32_t old = 0;
+          if (lane == 0) old = atomicAdd(&P.cnt_next[sbh], 1u);
+          old = __shfl_sync(0xffffffffu, old, 0);
+          if (old == (uint32_t)(QK / ROWS - 1)) {
+            __threadfence();
+            prep_superblock<float>(P.out, P.rows, P.m, NT, sbh, P.next, true);
+            if (lane == 0) P.cnt_next[sbh] = 0u;
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[a][n][0] = acc[a][n][1] = 0.f;
+      cu += WARPS;
+      if (cu < u1) {
+        crt = (int)(cu % nrt);
+        cks = (int)(cu / nrt);
+        csb = cks * P.kc;
+        csb_end = min(P.nsb, csb + P.kc);
+      }
+    }
+  }
+  if (failed) {
+    // let copies already in flight land before the CTA's shared memory goes away
+    for (int s = step; s < issued; ++s) (void)mbar_wait(&bar[s % STAGES], (uint32_t)(s / STAGES) & 1u, nullptr);
+  }
+}
+
+constexpr int WARPS = 8;
+constexpr int STAGES1 = 4;  // K1 stages per warp (2 x 16 rows x 144 B each)
+constexpr int STAGES2 = 6;  // K2 stages per warp (16 rows x 144 B each)
+
+template <int NMAT, int NT, int STAGES>
+cudaError_t launch_gemv(const GemvParams& P, int grid, cudaStream_t s) {
+  auto kern = gemv_kernel<NMAT, NT, STAGES, WARPS>;
+  const size_t smem = (size_t)WARPS * STAGES * (NMAT * 16 * BLK + 8);
+  static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_set >> dev & 1)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+// Choose the number of K-splits: the fewest that keep the per-CTA unit counts
+// within ~7% of each other.
+void choose_split(int nsb, int nrt, int grid, int* nks_out, int* kc_out) {
+  double best_eff = -1;
+  int best_nks = 1, best_kc = nsb;
+  for (int t = 1; t <= nsb; ++t) {
+    const int kc = (nsb + t - 1) / t;
+    const int nks = (nsb + kc - 1) / kc;
+    const double per = (double)nks * nrt / grid;
+    const double eff = per / std::ceil(per);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best_nks = nks;
+      best_kc = kc;
+    }
+    if (eff >= 0.93) break;
+  }
+  *nks_out = best_nks;
+  *kc_out = best_kc;
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+}  // namespace
+
+bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p) {
+  if (m < 1 || m > 8) return false;
+  p->m = (int)m;
+  p->hidden = (int)hidden;
+  p->inter = (int)inter;
+  p->nt = (int)((m + 3) / 4);
+  const int nsb1 = (int)(hidden / QK), nsb2 = (int)(inter / QK);
+  const int nrt1 = (int)(inter / 16), nrt2 = (int)(hidden / 16);
+  choose_split(nsb1, nrt1, num_sms, &p->nks1, &p->kc1);
+  choose_split(nsb2, nrt2, num_sms, &p->nks2, &p->kc2);
+  p->grid1 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks1 * nrt1);
+  p->grid2 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks2 * nrt2);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  p->off_fx1 = take((size_t)nsb1 * 16 * p->nt * 32 * 8);
+  p->off_fm1 = take((size_t)nsb1 * p->nt * 32 * 4);
+  p->off_sc1 = take((size_t)nsb1 * 8 * 4);
+  p->off_fx2 = take((size_t)nsb2 * 16 * p->nt * 32 * 8);
+  p->off_fm2 = take((size_t)nsb2 * p->nt * 32 * 4);
+  p->off_sc2 = take((size_t)nsb2 * 8 * 4);
+  p->off_h = take((size_t)m * inter * 4);
+  p->off_p1 = take(p->nks1 > 1 ? (size_t)p->nks1 * 2 * m * inter * 4 : 0);
+  p->off_p2 = take(p->nks2 > 1 ? (size_t)p->nks2 * m * hidden * 4 : 0);
+  p->off_sem1 = take((size_t)nrt1 * 4);
+  p->off_cnt2 = take((size_t)nsb2 * 4);
+  p->off_sem2 = take((size_t)nrt2 * 4);
+  p->ws_bytes = o;
+  return true;
+}
+
+cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
+                          float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof) {
+  uint8_t* W = (uint8_t*)ws;
+  FragPtrs f1{(uint2*)(W + p.off_fx1), (uint32_t*)(W + p.off_fm1), (float*)(W + p.off_sc1)};
+  FragPtrs f2{(uint2*)(W + p.off_fx2), (uint32_t*)(W + p.off_fm2), (float*)(W + p.off_sc2)};
+  const int nsb1 = p.hidden / QK;
+  // K0: not a dependent launch, so it also orders this call after the previous one on the stream
+  uint32_t* counters = (uint32_t*)(W + p.off_sem1);
+  const int ncounters = (int)((p.ws_bytes - p.off_sem1) / 4);
+  prof.before(0, s);
+  if (bf16)
+    prep_x_kernel<__nv_bfloat16>
+        <<<nsb1, 32, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
+  else
+    prep_x_kernel<float><<<nsb1, 32, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
+  prof.after(0, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  GemvParams g1{};
+  g1.w0 = (const uint8_t*)wg;
+  g1.w1 = (const uint8_t*)wu;
+  g1.rows = p.inter;
+  g1.nsb = nsb1;
+  g1.m = p.m;
+  g1.kc = p.kc1;
+  g1.nks = p.nks1;
+  g1.in = f1;
+  g1.part = (float*)(W + p.off_p1);
+  g1.sem = (uint32_t*)(W + p.off_sem1);
+  g1.out = (float*)(W + p.off_h);
+  g1.next = f2;
+  g1.cnt_next = (uint32_t*)(W + p.off_cnt2);
+  g1.err = err;
+  prof.before(1, s);
+  e = (p.nt == 1) ? launch_gemv<2, 1, STAGES1>(g1, p.grid1, s) : launch_gemv<2, 2, STAGES1>(g1, p.grid1, s);
+  prof.after(1, s);
+  if (e != cudaSuccess) return e;
+
+  GemvParams g2{};
+  g2.w0 = (const uint8_t*)wd;
+  g2.w1 = nullptr;
+  g2.rows = p.hidden;
+  g2.nsb = p.inter / QK;
+  g2.m = p.m;
+  g2.kc = p.kc2;
+  g2.nks = p.nks2;
+  g2.in = f2;
+  g2.part = (float*)(W + p.off_p2);
+  g2.sem = (uint32_t*)(W + p.off_sem2);
+  g2.out = y;
+  g2.err = err;
+  prof.before(2, s);
+  e = (p.nt == 1) ? launch_gemv<1, 1, STAGES2>(g2, p.grid2, s) : launch_gemv<1, 2, STAGES2>(g2, p.grid2, s);
+  prof.after(2, s);
+  return e;
+}
+
+}  // namespace q4k

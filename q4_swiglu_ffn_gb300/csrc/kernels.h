@@ -1,0 +1,51 @@
+// Host-side launch interface of the sm_103a kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace q4k {
+
+// Optional per-kernel timing: when ev != nullptr, the FFN launchers record
+// ev[2i] before and ev[2i+1] after their i-th kernel (i < n / 2) on the call's stream.
+struct ProfileEvents {
+  cudaEvent_t* ev = nullptr;
+  int n = 0;
+  void before(int i, cudaStream_t s) const { if (ev && 2 * i + 1 < n) cudaEventRecord(ev[2 * i], s); }
+  void after(int i, cudaStream_t s) const { if (ev && 2 * i + 1 < n) cudaEventRecord(ev[2 * i + 1], s); }
+};
+
+cudaError_t launch_dequant(const void* w, float* out, int64_t rows, int64_t cols, cudaStream_t s);
+cudaError_t launch_q8_1(const void* x, int bf16, int64_t m, int64_t k, void* out, cudaStream_t s);
+cudaError_t launch_quantize_weights(const void* w, int bf16, int64_t rows, int64_t cols, void* out,
+                                    uint32_t* err, cudaStream_t s);
+
+// ---------------------------------------------------------------- decode (m <= 8)
+struct DecodePlan {
+  int m, hidden, inter;
+  int nt;              // n-tiles of 4 tokens (1 or 2)
+  int nks1, kc1;       // gate/up K-splits and superblocks per split
+  int nks2, kc2;       // down K-splits
+  int grid1, grid2;    // CTAs
+  size_t ws_bytes;     // workspace bytes
+  // workspace offsets (bytes)
+  size_t off_fx1, off_fm1, off_sc1, off_fx2, off_fm2, off_sc2, off_h, off_p1, off_p2, off_sem1, off_cnt2,
+      off_sem2;
+};
+bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p);
+cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
+                          float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
+
+// ---------------------------------------------------------------- prefill (m >= 9)
+struct PrefillPlan {
+  int m, hidden, inter;
+  size_t ws_bytes;
+  size_t off_xq, off_hq;  // planar Q8_1 of x and of h
+  size_t off_xop, off_hop;  // tensor-core operands
+  size_t off_misc;
+};
+bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);
+cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
+                           const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
+                           const ProfileEvents& prof);
+
+}  // namespace q4k

@@ -1,0 +1,617 @@
+// Prefill regime (m >= 9 tokens) of the Q4_K SwiGLU FFN on sm_103a.
+//
+//   P0 q8_1(x)             x -> planar Q8_1 (bit-exact; also the ABI's q8_1_quantize_act)
+//   P1 expand(xq)          Q8_1 -> tensor-core B operand planes (below)
+//   P2 mmq<gate/up>        G = deq(Wg) . deq(xq), U = deq(Wu) . deq(xq) on tcgen05,
+//                          h = silu(G) * U, h -> planar Q8_1 (hq)
+//   P3 expand(hq)
+//   P4 mmq<down>           y = deq(Wd) . deq(hq), float32
+// Source: spark_model/layers/ops/q4k_mmq.rs (per-prefill activations to Q8_1,
+// then the Q4_K MMQ GEMM C[m, n] = A_q8[m, k] x W_q4k[n, k]); realizar
+// layers/ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (x quantized to Q8_1 once for
+// gate and up; the activated vector quantized again before down).
+//
+// Arithmetic. GB300's int8 tensor path (mma.sync s8) is slow and tcgen05 has no
+// integer kind on sm_103a, so the Q4_K x Q8_1 products run on tcgen05.mma
+// kind::f16 with operands that carry the integers exactly:
+//   A (weights, M = 128 rows):  q * scale_j as fp16 (<= 945, exact), unpacked from
+//                               the 4-bit quants by transform warps straight into
+//                               the 128-byte-swizzled shared-memory layout.
+//   B (activations, N = 128):   v = q8 * d8 * 2^-e_t split into fp16 hi and lo
+//                               (about 22 bits of v; e_t per token keeps |v| < 2^15).
+// Each superblock (256 k) accumulates into its own TMEM buffer; the epilogue
+// warps add d * D_main - 64*dmin * D_min into registers, where D_min is one
+// K = 16 MMA of the 6-bit mins against s8_j * 2^-(e_t+6) (hi and lo), s8_j =
+// d8_j * sum(q8) of sub-block j. The closed form per output is
+//   sum_b [ d_b * sum_j scale_j * sum_i q_i * v_i  -  dmin_b * sum_j min_j * s8_j ],
+// i.e. the dot product of the dequantized Q4_K row with the dequantized Q8_1
+// activations. The k order inside every aligned group of 8 is (0,2,1,3,4,6,5,7)
+// on both operands, which is the order the nibble unpacking produces.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace q4k {
+
+namespace {
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// ------------------------------------------------------------------------- expand
+// One CTA (256 threads) per token row. Writes
+//   hi[t][k], lo[t][k]  fp16 planes of q8*d8*2^-e_t at permuted positions,
+//   mn[t][sb*64 + 0..15] fp16 of s8_j*2^-(e_t+6): hi of the 8 sub-blocks, then lo,
+//   scale[t] = 2^e_t.
+// e_t = exponent(127 * max_j d8_j) - 14.
+__device__ __forceinline__ int perm8(int i) { return (i == 1 || i == 5) ? i + 1 : (i == 2 || i == 6) ? i - 1 : i; }
+
+__global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ qs, const float2* __restrict__ ds,
+                                                     int k, __half* __restrict__ hi, __half* __restrict__ lo,
+                                                     __half* __restrict__ mn, float* __restrict__ scale) {
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const int nblk = k / Q8B;
+  const float2* dsr = ds + (int64_t)t * nblk;
+  float mx = 0.f;
+  for (int j = tid; j < nblk; j += 256) mx = fmaxf(mx, fabsf(dsr[j].x));
+  mx = warp_max(mx);
+  __shared__ float red[8];
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  int e = 0;
+  const float top = mx * 127.f;
+  if (top > 0.f) e = max((int)((__float_as_uint(top) >> 23) & 0xFF) - 127 - 14, -100);
+  const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  if (tid == 0) scale[t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  const int8_t* qr = qs + (int64_t)t * k;
+  __half* hr = hi + (int64_t)t * k;
+  __half* lr = lo ? lo + (int64_t)t * k : nullptr;
+  __half* mr = mn + (int64_t)t * (k / QK) * 64;
+  const int lane = tid & 31;
+  for (int base = 0; base < k; base += 2048) {
+    const int c = base + tid * 8;  // 8 values; one warp covers one superblock
+    if (c >= k) break;             // k % 256 == 0, so whole warps leave together
+    const float d8 = dsr[c / Q8B].x;
+    const float d8s = d8 * s;  // exact power-of-two scaling
+    const uint2 raw = *reinterpret_cast<const uint2*>(qr + c);
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[i] = (int)(int8_t)((raw.x >> (8 * i)) & 0xFF);
+      q[4 + i] = (int)(int8_t)((raw.y >> (8 * i)) & 0xFF);
+    }
+    __align__(16) __half vh[8], vl[8];
+    int qsum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int src = perm8(i);
+      const float v = (float)q[src] * d8s;
+      const __half h = __float2half_rn(v);
+      vh[i] = h;
+      vl[i] = __float2half_rn(fmaf((float)q[src], d8s, -__half2float(h)));
+      qsum += q[i];
+    }
+    *reinterpret_cast<uint4*>(hr + c) = *reinterpret_cast<uint4*>(vh);
+    if (lr) *reinterpret_cast<uint4*>(lr + c) = *reinterpret_cast<uint4*>(vl);
+    // sub-block sums: 4 lanes per Q8_1 block
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    const float d8m = d8s * 0.015625f;  // 2^-(e+6)
+    const float sv = (float)qsum * d8m;
+    const __half sh = __float2half_rn(sv);
+    const __half sl = __float2half_rn(fmaf((float)qsum, d8m, -__half2float(sh)));
+    // lane 4j holds sub-block j of this superblock
+    __half* ms = mr + (int64_t)(c / QK) * 64;
+    if ((lane & 3) == 0) {
+      ms[lane >> 2] = sh;
+      ms[8 + (lane >> 2)] = sl;
+    }
+    if (lane >= 16) ms[lane] = __float2half_rn(0.f);
+    if (lane < 16) ms[32 + lane] = __float2half_rn(0.f), ms[48 + lane] = __float2half_rn(0.f);
+  }
+}
+
+// ------------------------------------------------------------------------- tcgen05 MMQ
+constexpr int TM = 128;                   // weight rows per tile
+constexpr int TN = 128;                   // tokens per tile
+constexpr int KCH = 64;                   // k per chunk (one 128-byte swizzle atom of fp16)
+constexpr int CH_PER_SB = 5;              // 4 main chunks + 1 min chunk per superblock
+constexpr int STAGES = 4;
+constexpr int TILE_BYTES = TM * KCH * 2;  // 16 KB
+constexpr int STAGE_BYTES = 3 * TILE_BYTES;
+constexpr int NWARPS = 10;                // 0 TMA, 1 MMA, 2-5 transform, 6-9 epilogue
+constexpr int W_TMA = 0, W_MMA = 1, W_XF = 2, W_EPI = 6;
+constexpr uint32_t TMEM_COLS = 512;       // D_main[2] at 0/128, D_min[2] at 256/384
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+
+struct MmqParams {
+  const uint8_t* w0;   // gate (gate/up kernel) or down
+  const uint8_t* w1;   // up (gate/up kernel)
+  int nsb;             // superblocks along K
+  int m;               // tokens
+  int ldo;             // output row length (inter for hq, hidden for y)
+  int ntn;             // tiles along N (tokens)
+  const float* tscale; // 2^e_t per token
+  int8_t* hq_qs;       // gate/up: Q8_1 quants of h [m][inter]
+  float2* hq_ds;       // gate/up: Q8_1 (d, s) of h [m][inter/32]
+  float* y;            // down: [m][hidden]
+  uint32_t* err;
+};
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  // K-major, 128-byte swizzle, 8-row atoms 1024 bytes apart (SBO), version 1 (sm_100 family)
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// kind::f16, fp16 A and B, fp32 D, both K-major, N = TN, M = TM
+constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(IDESC), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bounded wait that also gives up when another role has already aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+      set_error(err, ERRBIT_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(NWARPS * 32, 1)
+    mmq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constant__ CUtensorMap tm_lo,
+               const __grid_constant__ CUtensorMap tm_mn, const MmqParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* accf = empty + STAGES;
+  uint64_t* acce = accf + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x % P.ntn, mt = blockIdx.x / P.ntn;
+  const int64_t rowbytes = (int64_t)P.nsb * BLK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 5);   // 4 transform warps + the TMA producer
+      mbar_init(&empty[s], 1);  // one tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);   // tcgen05.commit
+      mbar_init(&acce[b], 4);   // 4 epilogue warps
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == W_MMA) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nchunks = P.nsb * CH_PER_SB;
+
+  if (warp == W_TMA) {
+    // ------------------------------------------------------------ TMA producer (B operand)
+    if (lane == 0) {
+      for (int q = 0; q < nchunks; ++q) {
+        const int s = q % STAGES, u = q / STAGES;
+        if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) break;
+        uint8_t* st = smem + s * STAGE_BYTES;
+        const int sb = q / CH_PER_SB, c = q % CH_PER_SB;
+        if (c < 4) {
+          mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
+          tma_load_2d(st + TILE_BYTES, &tm_hi, sb * QK + c * KCH, nt * TN, &full[s]);
+          tma_load_2d(st + 2 * TILE_BYTES, &tm_lo, sb * QK + c * KCH, nt * TN, &full[s]);
+        } else {
+          mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+          tma_load_2d(st + TILE_BYTES, &tm_mn, sb * KCH, nt * TN, &full[s]);
+        }
+      }
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int sb = 0; sb < P.nsb && !*abort_flag; ++sb) {
+        const int ab = sb & 1;
+        if (sb >= 2 && !wait_bar(&acce[ab], ((sb - 2) >> 1) & 1, abort_flag, P.err)) break;
+        tc_fence_after();
+        const uint32_t d_main = tmem + ab * TN, d_min = tmem + 256 + ab * TN;
+        bool ok = true;
+        for (int c = 0; c < CH_PER_SB; ++c) {
+          const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
+          if (!wait_bar(&full[s], u & 1, abort_flag, P.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          const uint64_t a = sw128_desc(st), b0 = sw128_desc(st + TILE_BYTES), b1 = sw128_desc(st + 2 * TILE_BYTES);
+          if (c < 4) {
+#pragma unroll
+            for (int ks = 0; ks < KCH / 16; ++ks) {
+              const uint64_t off = (uint64_t)((ks * 32) >> 4);  // 16 fp16 = 32 bytes along K
+              mma_f16(d_main, a + off, b0 + off, (c | ks) != 0);
+              mma_f16(d_main, a + off, b1 + off, 1u);
+            }
+          } else {
+            mma_f16(d_min, a, b0, 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&accf[ab]);
+      }
+    }
+  } else if (warp < W_EPI) {
+    // ------------------------------------------------------------ transform: Q4_K -> fp16 A tiles
+    const int r = threadIdx.x - W_XF * 32;  // tile row 0..127
+    const uint8_t* src;
+    if (GATEUP)
+      src = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
+    else
+      src = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
+    const uint32_t rsw = (uint32_t)(r & 7);
+    uint8_t* arow_base = smem + (r >> 3) * 1024 + (r & 7) * 128;  // + stage offset
+    uint4 raw[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+    bool ok = true;
+    for (int sb = 0; sb < P.nsb && ok; ++sb) {
+      uint4 cur[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) cur[i] = raw[i];
+      if (sb + 1 < P.nsb) {
+#pragma unroll
+        for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(sb + 1) * BLK) + i);
+      }
+      const uint4 hd = cur[0];
+      for (int c = 0; c < CH_PER_SB; ++c) {
+        const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
+        if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) { ok = false; break; }
+        uint8_t* arow = arow_base + s * STAGE_BYTES;
+        if (c < 4) {
+          uint32_t sl, ml, sh, mh;
+          scale_min(hd.y, hd.z, hd.w, 2 * c, sl, ml);
+          scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sh, mh);
+          const __half2 mlo = __float2half2_rn((float)sl), alo = __float2half2_rn(-1024.f * (float)sl);
+          const __half2 mhi = __float2half2_rn((float)sh * 0.0625f), ahi = __float2half2_rn(-64.f * (float)sh);
+          const uint4 ga = cur[1 + 2 * c], gb = cur[2 + 2 * c];
+          const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint32_t w0 = wds[2 * p], w1 = wds[2 * p + 1];
+            const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
+            uint4 lo4, hi4;
+            lo4.x = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            lo4.y = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            lo4.z = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            lo4.w = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            hi4.x = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            hi4.y = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            hi4.z = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            hi4.w = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            *reinterpret_cast<uint4*>(arow + (((uint32_t)p ^ rsw) << 4)) = lo4;
+            *reinterpret_cast<uint4*>(arow + (((uint32_t)(4 + p) ^ rsw) << 4)) = hi4;
+          }
+        } else {
+          uint32_t mm[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t sc_;
+            scale_min(hd.y, hd.z, hd.w, j, sc_, mm[j]);
+          }
+          uint4 v;
+          v.x = h2_as_u32(__halves2half2(__uint2half_rn(mm[0]), __uint2half_rn(mm[1])));
+          v.y = h2_as_u32(__halves2half2(__uint2half_rn(mm[2]), __uint2half_rn(mm[3])));
+          v.z = h2_as_u32(__halves2half2(__uint2half_rn(mm[4]), __uint2half_rn(mm[5])));
+          v.w = h2_as_u32(__halves2half2(__uint2half_rn(mm[6]), __uint2half_rn(mm[7])));
+          *reinterpret_cast<uint4*>(arow + ((0u ^ rsw) << 4)) = v;
+          *reinterpret_cast<uint4*>(arow + ((1u ^ rsw) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const uint8_t* hdr;
+    if (GATEUP)
+      hdr = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
+    else
+      hdr = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
+    float acc[TN];
+#pragma unroll
+    for (int i = 0; i < TN; ++i) acc[i] = 0.f;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    bool ok = true;
+    for (int sb = 0; sb < P.nsb; ++sb) {
+      const int ab = sb & 1;
+      const uint32_t dm2 = __ldg(reinterpret_cast<const uint32_t*>(hdr + (int64_t)sb * BLK));
+      const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
+      if (!wait_bar(&accf[ab], (sb >> 1) & 1, abort_flag, P.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t tm_main = tmem + lane_addr + ab * TN, tm_min = tmem + lane_addr + 256 + ab * TN;
+#pragma unroll
+      for (int j = 0; j < TN / 16; ++j) {
+        float v[16], w[16];
+        tmem_ld16(tm_main + j * 16, v);
+        tmem_ld16(tm_min + j * 16, w);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(w[i], dmn, fmaf(v[i], d, acc[j * 16 + i]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[ab]);
+    }
+    const int t0 = nt * TN;
+    if (GATEUP) {
+      // exchange through the idle stage buffers: rows 0-63 hold gate, 64-127 up,
+      // for the same 64 inter indices. Every epilogue warp reaches the barrier.
+      float* xg = reinterpret_cast<float*>(smem);  // [128 rows][TN + 1]
+      constexpr int LD = TN + 1;
+      if (ok) {
+#pragma unroll
+        for (int i = 0; i < TN; ++i) {
+          const int t = t0 + i;
+          const float sc = t < P.m ? P.tscale[t] : 0.f;
+          xg[r * LD + i] = acc[i] * sc;
+        }
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (ok && !*abort_flag) {
+        const int ew = warp - W_EPI;          // 0..3
+        const int qb = ew & 1;                // Q8_1 block: inter rows 32*qb .. +31 of the tile
+        const int tbeg = (ew >> 1) * (TN / 2);
+        const int irow = mt * 64 + qb * 32 + lane;
+        for (int i = tbeg; i < tbeg + TN / 2; ++i) {
+          const int t = t0 + i;
+          if (t >= P.m) break;
+          const float g = xg[(qb * 32 + lane) * LD + i], u = xg[(64 + qb * 32 + lane) * LD + i];
+          const float h = silu_f(g) * u;
+          const float amax = warp_max(fabsf(h));
+          const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
+          const float dq = nz ? __fdiv_rn(amax, 127.f) : 0.f;
+          const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
+          float rq = roundf(__fmul_rn(h, inv));
+          rq = fminf(fmaxf(rq, -127.f), 127.f);
+          int qi = (int)rq, sum = qi;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+          P.hq_qs[(int64_t)t * P.ldo + irow] = (int8_t)qi;
+          if (lane == 0) P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq, __fmul_rn(dq, (float)sum));
+        }
+      }
+    } else if (ok) {
+      const int row = mt * TM + r;
+#pragma unroll
+      for (int i = 0; i < TN; ++i) {
+        const int t = t0 + i;
+        if (t < P.m) P.y[(int64_t)t * P.ldo + row] = acc[i] * P.tscale[t];
+      }
+    }
+  }
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let copies and MMAs already in flight land before the shared memory and TMEM go away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == W_MMA) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D fp16 tensor [rows][cols] (row-major), box 64 x 128, 128-byte swizzle; rows beyond
+// `rows` read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)KCH, (cuuint32_t)TN};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GATEUP>
+cudaError_t launch_mmq(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& mn, const MmqParams& P,
+                       int grid, cudaStream_t s) {
+  auto kern = mmq_kernel<GATEUP>;
+  static uint64_t attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !(attr_set >> dev & 1)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set |= 1ull << dev;
+  }
+  kern<<<grid, NWARPS * 32, SMEM_BYTES, s>>>(hi, lo, mn, P);
+  return cudaGetLastError();
+}
+
+struct Operand {
+  __half *hi, *lo, *mn;
+  float* scale;
+};
+
+}  // namespace
+
+bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p) {
+  (void)num_sms;
+  if (m < 9) return false;
+  p->m = (int)m;
+  p->hidden = (int)hidden;
+  p->inter = (int)inter;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  auto op_bytes = [&](int64_t k, bool with_lo) {
+    return align256((size_t)m * k * 2) * (with_lo ? 2 : 1) + align256((size_t)m * (k / QK) * 64 * 2) +
+           align256((size_t)m * 4);
+  };
+  p->off_xq = take((size_t)m * hidden + (size_t)m * (hidden / Q8B) * 8);
+  p->off_hq = take((size_t)m * inter + (size_t)m * (inter / Q8B) * 8);
+  p->off_xop = take(op_bytes(hidden, true));
+  p->off_hop = take(op_bytes(inter, true));
+  p->off_misc = take(256);
+  p->ws_bytes = o;
+  return true;
+}
+
+cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
+                           const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
+                           const ProfileEvents& prof) {
+  uint8_t* W = (uint8_t*)ws;
+  const int64_t m = p.m, H = p.hidden, I = p.inter;
+  auto split = [&](uint8_t* base, int64_t k, bool with_lo) {
+    Operand op;
+    size_t o = 0;
+    op.hi = (__half*)(base + o);
+    o += align256((size_t)m * k * 2);
+    op.lo = with_lo ? (__half*)(base + o) : nullptr;
+    if (with_lo) o += align256((size_t)m * k * 2);
+    op.mn = (__half*)(base + o);
+    o += align256((size_t)m * (k / QK) * 64 * 2);
+    op.scale = (float*)(base + o);
+    return op;
+  };
+  const Operand xo = split(W + p.off_xop, H, true);
+  const Operand ho = split(W + p.off_hop, I, true);
+  int8_t* xq = (int8_t*)(W + p.off_xq);
+  float2* xds = (float2*)(W + p.off_xq + (size_t)m * H);
+  int8_t* hq = (int8_t*)(W + p.off_hq);
+  float2* hds = (float2*)(W + p.off_hq + (size_t)m * I);
+
+  CUtensorMap mx_hi, mx_lo, mx_mn, mh_hi, mh_lo, mh_mn;
+  if (!make_map(&mx_hi, xo.hi, m, H) || !make_map(&mx_lo, xo.lo, m, H) ||
+      !make_map(&mx_mn, xo.mn, m, (H / QK) * 64) || !make_map(&mh_hi, ho.hi, m, I) ||
+      !make_map(&mh_lo, ho.lo, m, I) || !make_map(&mh_mn, ho.mn, m, (I / QK) * 64))
+    return cudaErrorInvalidValue;
+
+  prof.before(0, s);
+  cudaError_t e = launch_q8_1(x, bf16, m, H, xq, s);
+  prof.after(0, s);
+  if (e != cudaSuccess) return e;
+  prof.before(1, s);
+  expand_kernel<<<(unsigned)m, 256, 0, s>>>(xq, xds, (int)H, xo.hi, xo.lo, xo.mn, xo.scale);
+  prof.after(1, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const int ntn = (int)((m + TN - 1) / TN);
+  MmqParams g{};
+  g.w0 = (const uint8_t*)wg;
+  g.w1 = (const uint8_t*)wu;
+  g.nsb = (int)(H / QK);
+  g.m = (int)m;
+  g.ldo = (int)I;
+  g.ntn = ntn;
+  g.tscale = xo.scale;
+  g.hq_qs = hq;
+  g.hq_ds = hds;
+  g.err = err;
+  prof.before(2, s);
+  e = launch_mmq<true>(mx_hi, mx_lo, mx_mn, g, (int)(I / 64) * ntn, s);
+  prof.after(2, s);
+  if (e != cudaSuccess) return e;
+
+  prof.before(3, s);
+  expand_kernel<<<(unsigned)m, 256, 0, s>>>(hq, hds, (int)I, ho.hi, ho.lo, ho.mn, ho.scale);
+  prof.after(3, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  MmqParams dn{};
+  dn.w0 = (const uint8_t*)wd;
+  dn.nsb = (int)(I / QK);
+  dn.m = (int)m;
+  dn.ldo = (int)H;
+  dn.ntn = ntn;
+  dn.tscale = ho.scale;
+  dn.y = y;
+  dn.err = err;
+  prof.before(4, s);
+  e = launch_mmq<false>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn, s);
+  prof.after(4, s);
+  return e;
+}
+
+}  // namespace q4k

@@ -8,3 +8,11 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103) and the built library")
+
+
+def pytest_sessionstart(session):
+    """GPU runs build the library first (the build is incremental and takes seconds)."""
+    markexpr = session.config.getoption("markexpr", "") or ""
+    if "gpu" in markexpr and "not gpu" not in markexpr:
+        import __graft_entry__
+        __graft_entry__._build_module().build()

@@ -1,0 +1,92 @@
+"""Parity of the decode path (m <= 8) with the oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.gpu_util import dev, guarded_f32, guards_intact, lib, rel_l2, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+
+# Acceptance bound (BASELINE): L2-relative error <= 1e-3. The decode arithmetic
+# (fp16 hi+lo activations, ~2^-22 relative, exact q*scale, fp32 accumulation)
+# sits far below it; DECODE_TIGHT catches a slip the acceptance bound would hide.
+ACCEPT = 1e-3
+DECODE_TIGHT = 2e-5
+
+
+def _run(cfg, x=None, m=None):
+    wg, wu, wd = workloads.weights(cfg)
+    if x is None:
+        x, _ = workloads.activations(cfg, m=m)
+    m, H = x.shape
+    buf, y = guarded_f32(m * H)
+    lib().ffn_q4k_swiglu(to_dev(x), to_dev(wg), to_dev(wu), to_dev(wd), y=y.view(m, H))
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    ref, _ = oracle.ffn_decode(x, wg, wu, wd)
+    return y.view(m, H).cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("cfg_index", [0, 1, 2])
+def test_decode_workloads(cfg_index):
+    y, ref = _run(workloads.CONFIGS[cfg_index])
+    err = rel_l2(y, ref)
+    assert err <= ACCEPT and err <= DECODE_TIGHT, err
+    assert lib().q4k_check_device_error() == 0
+
+
+@pytest.mark.parametrize("H,I,m", [(256, 256, 1), (256, 512, 2), (512, 256, 3), (768, 1280, 4), (1024, 768, 5),
+                                   (2304, 1792, 6), (1280, 3328, 7), (4096, 2048, 8), (256, 4352, 8),
+                                   (6912, 512, 1)])
+def test_decode_shape_sweep(H, I, m):
+    c = workloads.small_config(H, I, m, "f32", ("channels", 0.01, 50.0))
+    y, ref = _run(c)
+    err = rel_l2(y, ref)
+    assert err <= DECODE_TIGHT, err
+
+
+def test_decode_repeatable_and_deterministic():
+    c = workloads.small_config(1024, 2816, 8)
+    wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
+    x, _ = workloads.activations(c)
+    xd = to_dev(x)
+    y1 = lib().ffn_q4k_swiglu(xd, wg, wu, wd).cpu().numpy()
+    y2 = lib().ffn_q4k_swiglu(xd, wg, wu, wd).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_decode_special_inputs():
+    c = workloads.small_config(512, 768, 3)
+    wg, wu, wd = workloads.weights(c)
+    # zero input -> exactly zero output
+    y = lib().ffn_q4k_swiglu(to_dev(np.zeros((3, 512), np.float32)), to_dev(wg), to_dev(wu), to_dev(wd))
+    assert np.all(y.cpu().numpy() == 0)
+    # huge and tiny activations in one token (exercise the per-superblock exponent)
+    x = np.zeros((3, 512), np.float32)
+    x[0] = workloads.normal(5, 1, 512) * 1e4
+    x[1] = workloads.normal(5, 2, 512) * 1e-6
+    x[2, ::7] = 3.0e5
+    y, ref = _run(c, x=x)
+    assert rel_l2(y, ref) <= DECODE_TIGHT
+
+
+def test_decode_bf16_input_through_ex():
+    c = workloads.small_config(768, 1024, 4, "bf16", ("channels", 0.01, 100.0))
+    wg, wu, wd = workloads.weights(c)
+    xf, xb = workloads.activations(c)
+    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(4, 768, 1024), dtype=torch.uint8, device=dev())
+    y = lib().ffn_q4k_swiglu_ex(to_dev(xb), to_dev(wg), to_dev(wu), to_dev(wd), ws)
+    ref, _ = oracle.ffn_decode(xf, wg, wu, wd)
+    assert rel_l2(y.cpu().numpy(), ref) <= DECODE_TIGHT
+
+
+def test_workspace_too_small_is_rejected():
+    c = workloads.small_config(256, 512, 1)
+    wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
+    x = to_dev(np.ones((1, 256), np.float32))
+    need = lib().ffn_q4k_workspace_bytes(1, 256, 512)
+    ws = torch.zeros(need - 256, dtype=torch.uint8, device=dev())
+    with pytest.raises(lib().Q4KError) as e:
+        lib().ffn_q4k_swiglu_ex(x, wg, wu, wd, ws)
+    assert e.value.status == 8

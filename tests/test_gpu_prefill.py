@@ -1,0 +1,99 @@
+"""Parity of the prefill path (m >= 9: Q8_1 activations, tcgen05 Q4_K x Q8_1 GEMM) with the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests.gpu_util import dev, guarded_f32, guards_intact, lib, rel_l2, to_dev, torch
+
+pytestmark = pytest.mark.gpu
+
+ACCEPT = 1e-3          # acceptance bound: L2-relative error of y against the oracle
+DOWN_TIGHT = 1e-5      # y against the oracle's down stage fed the GPU's own Q8_1(h)
+HQ_FLIP_FRAC = 2e-3    # Q8_1(h) bytes may differ where h sits on a rounding boundary
+
+
+def _run(cfg, m=None, sample=None):
+    wg, wu, wd = workloads.weights(cfg)
+    xf, xb = workloads.activations(cfg, m=m)
+    m, H = xf.shape
+    I = cfg.inter
+    need = lib().ffn_q4k_workspace_bytes(m, H, I)
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev())
+    buf, y = guarded_f32(m * H)
+    lib().ffn_q4k_swiglu_ex(to_dev(xb), to_dev(wg), to_dev(wu), to_dev(wd), ws, y=y.view(m, H))
+    torch.cuda.synchronize()
+    assert guards_intact(buf)
+    assert lib().q4k_check_device_error() == 0
+    y = y.view(m, H).cpu().numpy()
+    off = lib().ffn_q4k_workspace_h_q8_1_offset(m, H, I)
+    hq_gpu = oracle.q8_1_from_bytes(ws[off:off + lib().q8_1_bytes(m, I)].cpu().numpy(), m, I)
+    rows = np.arange(m) if sample is None else sample
+    ref = oracle.ffn_prefill(xf[rows], wg, wu, wd)
+    return y[rows], ref, tuple(a[rows] for a in hq_gpu), wd
+
+
+def _check(y, ref, hq_gpu, wd):
+    err = rel_l2(y, ref["y"])
+    assert err <= ACCEPT, err
+    hq, hd, hs = ref["hq"]
+    gq, gd, gs = hq_gpu
+    flips = np.count_nonzero(gq != hq)
+    assert flips <= HQ_FLIP_FRAC * hq.size, flips
+    # a flip moves a value by at most one quant step of its block (blocks that are
+    # numerically zero, amax < 1e-30, may differ in any way)
+    dv = np.abs(oracle.dequantize_q8_1(gq, gd) - oracle.dequantize_q8_1(hq, hd))
+    step = np.repeat(np.maximum(gd, hd).astype(np.float64), 32, axis=1)
+    assert np.all(dv <= 1.01 * step + 1e-30 * 127)
+    # the down GEMM alone, fed the GPU's own Q8_1(h)
+    y_down = oracle.ffn_down_from_q8_1(gq, gd, wd)
+    assert rel_l2(y, y_down) <= DOWN_TIGHT
+    return err
+
+
+@pytest.mark.parametrize("H,I,m", [(256, 256, 9), (256, 512, 16), (512, 256, 127), (256, 768, 128),
+                                   (768, 512, 129), (1024, 1280, 200), (512, 2048, 257), (1280, 256, 64)])
+def test_prefill_shape_sweep(H, I, m):
+    c = workloads.small_config(H, I, m, "bf16", ("channels", 0.01, 100.0))
+    y, ref, hq, wd = _run(c)
+    _check(y, ref, hq, wd)
+
+
+def test_prefill_float32_input():
+    c = workloads.small_config(512, 768, 33, "f32", ("entries", 0.001, 900.0))
+    y, ref, hq, wd = _run(c)
+    _check(y, ref, hq, wd)
+
+
+def test_prefill_config3_full():
+    y, ref, hq, wd = _run(workloads.CONFIGS[3])
+    _check(y, ref, hq, wd)
+
+
+def test_prefill_config4_sampled_tokens():
+    """Full 2048-token run in the benchmark's launch configuration; 48 tokens checked."""
+    rng = np.random.default_rng(4)
+    sample = np.sort(rng.choice(2048, 48, replace=False))
+    sample[0], sample[-1] = 0, 2047
+    y, ref, hq, wd = _run(workloads.CONFIGS[4], sample=sample)
+    _check(y, ref, hq, wd)
+
+
+def test_prefill_zero_input():
+    c = workloads.small_config(256, 512, 20, "bf16")
+    wg, wu, wd = workloads.weights(c)
+    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(20, 256, 512), dtype=torch.uint8, device=dev())
+    x = torch.zeros((20, 256), dtype=torch.bfloat16, device=dev())
+    y = lib().ffn_q4k_swiglu_ex(x, to_dev(wg), to_dev(wu), to_dev(wd), ws)
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_prefill_repeatable():
+    c = workloads.small_config(512, 1024, 140, "bf16", ("channels", 0.01, 100.0))
+    wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
+    _, xb = workloads.activations(c)
+    xd = to_dev(xb)
+    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(140, 512, 1024), dtype=torch.uint8, device=dev())
+    y1 = lib().ffn_q4k_swiglu_ex(xd, wg, wu, wd, ws).cpu().numpy()
+    y2 = lib().ffn_q4k_swiglu_ex(xd, wg, wu, wd, ws).cpu().numpy()
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
