@@ -216,6 +216,10 @@ def gpu_decode(args, rank, world, dist):
     nk = 3
     P = 300
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
+    for ev in evs:
+        for e in ev:
+            e.record(stream)  # torch creates the CUDA event on first record
+    torch.cuda.synchronize()
     for i in range(P):
         q.q4k_set_profile_events(evs[i])
         step(i)
@@ -275,6 +279,10 @@ def gpu_prefill(args):
     nk = 5
     P = 10
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
+    for ev in evs:
+        for e in ev:
+            e.record(stream)  # torch creates the CUDA event on first record
+    torch.cuda.synchronize()
     for i in range(P):
         q.q4k_set_profile_events(evs[i])
         step()

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace q4k {
 
@@ -162,10 +163,54 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
+// Per-thread constants for reading the two sub-blocks (2*tig, 2*tig+1) a quad
+// thread owns out of the 12 packed scale/min bytes (s0, s1, s2 = bytes 0-3, 4-7,
+// 8-11): their bytes sit at positions bp, bp+1 (bp = 2*(tig&1)); sub-blocks
+// 4-7 (tig >= 2) take the low/high nibbles of bytes 8-11 plus the top two bits
+// of bytes 0-7.
+struct ScaleSel {
+  uint32_t shift;  // 8 * bp
+  bool high;       // tig >= 2
+};
+__device__ __forceinline__ void owned_scales(const ScaleSel& S, uint32_t s0, uint32_t s1, uint32_t s2,
+                                             uint32_t& sc_a, uint32_t& sc_b, uint32_t& m_a, uint32_t& m_b) {
+  const uint32_t w0 = s0 >> S.shift, w1 = s1 >> S.shift, w2 = s2 >> S.shift;
+  if (!S.high) {
+    sc_a = w0 & 63u;
+    sc_b = (w0 >> 8) & 63u;
+    m_a = w1 & 63u;
+    m_b = (w1 >> 8) & 63u;
+  } else {
+    sc_a = (w2 & 15u) | ((w0 >> 2) & 0x30u);
+    sc_b = ((w2 >> 8) & 15u) | ((w0 >> 10) & 0x30u);
+    m_a = ((w2 >> 4) & 15u) | ((w1 >> 2) & 0x30u);
+    m_b = ((w2 >> 12) & 15u) | ((w1 >> 10) & 0x30u);
+  }
+}
+// half2(v, v) for an integer 0 <= v < 1024, exactly: (1024 + v) - 1024 in fp16
+__device__ __forceinline__ __half2 small_int_h2(uint32_t v) {
+  return __hsub2(u32_as_h2(0x64006400u | (v * 0x00010001u)), u32_as_h2(0x64006400u));
+}
+__device__ __forceinline__ __half2 small_int_pair_h2(uint32_t a, uint32_t b) {
+  return __hsub2(u32_as_h2(0x64006400u | a | (b << 16)), u32_as_h2(0x64006400u));
+}
+
+__device__ __forceinline__ void tma_tile(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 template <int NMAT, int NT, int STAGES, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P) {
+__global__ void __launch_bounds__(WARPS * 32, 1)
+    gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+                const GemvParams P) {
   constexpr int ROWS = 16;
-  constexpr int STAGE_BYTES = NMAT * ROWS * BLK;
+  constexpr int MAT_BYTES = ROWS * BLK;  // one 16-row x 1-superblock tile
+  constexpr int STAGE_BYTES = NMAT * MAT_BYTES;
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   uint8_t* ring = smem + warp * STAGES * STAGE_BYTES;
@@ -182,7 +227,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
   }
   __syncwarp();
 
-  // issue cursor (which step the next bulk copy loads)
+  // issue cursor (which step the next tile load fetches)
   int64_t iu = u0 + warp;
   int isb = 0, isb_end = 0, irt = 0;
   if (iu < u1) {
@@ -194,13 +239,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
   auto issue = [&](int stage) {
     fence_proxy_async_smem();
     __syncwarp();
-    uint8_t* dst = ring + stage * STAGE_BYTES;
-    if (lane == 0) mbar_arrive_expect_tx(&bar[stage], STAGE_BYTES);
-    __syncwarp();
-    if (lane < NMAT * ROWS) {
-      const int mat = lane / ROWS, r = lane % ROWS;
-      const uint8_t* src = (mat ? P.w1 : P.w0) + ((int64_t)(irt * ROWS + r) * P.nsb + isb) * BLK;
-      bulk_g2s_hint(dst + lane * BLK, src, BLK, &bar[stage], pol);
+    if (lane == 0) {
+      uint8_t* dst = ring + stage * STAGE_BYTES;
+      mbar_arrive_expect_tx(&bar[stage], STAGE_BYTES);
+      tma_tile(dst, &tm0, isb * (BLK / 8), irt * ROWS, &bar[stage], pol);
+      if (NMAT == 2) tma_tile(dst + MAT_BYTES, &tm1, isb * (BLK / 8), irt * ROWS, &bar[stage], pol);
     }
     if (++isb == isb_end) {
       iu += WARPS;
@@ -216,6 +259,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
   for (; issued < STAGES - 1 && iu < u1; ++issued) issue(issued % STAGES);
   pdl_launch_dependents();
   pdl_wait();  // input fragments come from the previous kernel
+
+  const ScaleSel ssel{8u * 2u * (uint32_t)(tig & 1), tig >= 2};
 
   // consume cursor
   int64_t cu = u0 + warp;
@@ -254,29 +299,30 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
     for (int a = 0; a < NMAT; ++a) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const uint8_t* rb = st + (a * ROWS + g + 8 * r) * BLK;
+        const uint8_t* rb = st + a * MAT_BYTES + (g + 8 * r) * BLK;
         const uint4 hd = *reinterpret_cast<const uint4*>(rb);
         q0[a][r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
         q1[a][r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
-        dd[a][r] = fp16_bits_to_f32(hd.x);
-        dm[a][r] = fp16_bits_to_f32(hd.x >> 16);
-        uint32_t sl, ml, sh, mh;
-        scale_min(hd.y, hd.z, hd.w, 2 * tig, sl, ml);
-        scale_min(hd.y, hd.z, hd.w, 2 * tig + 1, sh, mh);
-        mlo[a][r] = __float2half2_rn((float)sl);
-        alo[a][r] = __float2half2_rn(-1024.f * (float)sl);
-        mhi[a][r] = __float2half2_rn((float)sh * 0.0625f);
-        ahi[a][r] = __float2half2_rn(-64.f * (float)sh);
-        A_min[a][r] = h2_as_u32(__halves2half2(__uint2half_rn(ml), __uint2half_rn(mh)));
+        const float2 dpair = __half22float2(u32_as_h2(hd.x));
+        dd[a][r] = dpair.x;
+        dm[a][r] = dpair.y;
+        uint32_t sa, sb, ma, mb;
+        owned_scales(ssel, hd.y, hd.z, hd.w, sa, sb, ma, mb);
+        mlo[a][r] = small_int_h2(sa);
+        alo[a][r] = __hmul2(mlo[a][r], u32_as_h2(0xE400E400u));  // * -1024
+        const __half2 shb = small_int_h2(sb);
+        mhi[a][r] = __hmul2(shb, u32_as_h2(0x2C002C00u));        // * 1/16
+        ahi[a][r] = __hmul2(shb, u32_as_h2(0xD400D400u));        // * -64
+        A_min[a][r] = h2_as_u32(small_int_pair_h2(ma, mb));
       }
     }
-    float c[NMAT][NT][4], cm[NMAT][NT][4];
+    float c[NMAT][NT][2][4], cm[NMAT][NT][4];
 #pragma unroll
     for (int a = 0; a < NMAT; ++a)
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) c[a][n][i] = cm[a][n][i] = 0.f;
+        for (int i = 0; i < 4; ++i) c[a][n][0][i] = c[a][n][1][i] = cm[a][n][i] = 0.f;
 
     const uint2* fx = P.in.fx + (int64_t)csb * 16 * NT * 32 + lane;
 #pragma unroll
@@ -302,8 +348,8 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
         }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          mma16816(c[a][n], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
-          mma16816(c[a][n], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
+          mma16816(c[a][n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
+          mma16816(c[a][n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
         }
       }
     }
@@ -323,7 +369,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1) gemv_kernel(const GemvParams P)
       for (int a = 0; a < NMAT; ++a) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-          const float main = c[a][n][2 * r] + c[a][n][2 * r + 1];
+          const float main = (c[a][n][0][2 * r] + c[a][n][1][2 * r]) + (c[a][n][0][2 * r + 1] + c[a][n][1][2 * r + 1]);
           const float mins = cm[a][n][2 * r] + cm[a][n][2 * r + 1];
           acc[a][n][r] = fmaf(main, dd[a][r] * xs, acc[a][n][r]);
           acc[a][n][r] = fmaf(-mins, dm[a][r] * (64.f * xs), acc[a][n][r]);
@@ -424,7 +470,8 @@ constexpr int STAGES1 = 4;  // K1 stages per warp (2 x 16 rows x 144 B each)
 constexpr int STAGES2 = 6;  // K2 stages per warp (16 rows x 144 B each)
 
 template <int NMAT, int NT, int STAGES>
-cudaError_t launch_gemv(const GemvParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
+                        cudaStream_t s) {
   auto kern = gemv_kernel<NMAT, NT, STAGES, WARPS>;
   const size_t smem = (size_t)WARPS * STAGES * (NMAT * 16 * BLK + 8);
   static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
@@ -446,7 +493,14 @@ cudaError_t launch_gemv(const GemvParams& P, int grid, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, P);
+  return cudaLaunchKernelEx(&cfg, kern, t0, t1, P);
+}
+
+// Weight matrix [rows][nsb blocks] as a 2-D tensor of 8-byte elements (18 per
+// block), loaded 16 rows x 1 superblock at a time.
+bool weight_map(CUtensorMap* m, const void* w, int rows, int nsb) {
+  return tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, w, (uint64_t)rows, (uint64_t)nsb * (BLK / 8),
+                 (uint64_t)nsb * BLK, BLK / 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Choose the number of K-splits: the fewest that keep the per-CTA unit counts
@@ -542,8 +596,13 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   g1.next = f2;
   g1.cnt_next = (uint32_t*)(W + p.off_cnt2);
   g1.err = err;
+  CUtensorMap mg, mu, md;
+  if (!weight_map(&mg, wg, p.inter, nsb1) || !weight_map(&mu, wu, p.inter, nsb1) ||
+      !weight_map(&md, wd, p.hidden, p.inter / QK))
+    return cudaErrorInvalidValue;
   prof.before(1, s);
-  e = (p.nt == 1) ? launch_gemv<2, 1, STAGES1>(g1, p.grid1, s) : launch_gemv<2, 2, STAGES1>(g1, p.grid1, s);
+  e = (p.nt == 1) ? launch_gemv<2, 1, STAGES1>(mg, mu, g1, p.grid1, s)
+                  : launch_gemv<2, 2, STAGES1>(mg, mu, g1, p.grid1, s);
   prof.after(1, s);
   if (e != cudaSuccess) return e;
 
@@ -561,7 +620,8 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   g2.out = y;
   g2.err = err;
   prof.before(2, s);
-  e = (p.nt == 1) ? launch_gemv<1, 1, STAGES2>(g2, p.grid2, s) : launch_gemv<1, 2, STAGES2>(g2, p.grid2, s);
+  e = (p.nt == 1) ? launch_gemv<1, 1, STAGES2>(md, md, g2, p.grid2, s)
+                  : launch_gemv<1, 2, STAGES2>(md, md, g2, p.grid2, s);
   prof.after(2, s);
   return e;
 }

@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 
 namespace q4k {
 
@@ -461,32 +462,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 }
 
 // ------------------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2-D fp16 tensor [rows][cols] (row-major), box 64 x 128, 128-byte swizzle; rows beyond
 // `rows` read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)KCH, (cuuint32_t)TN};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, (uint64_t)rows, (uint64_t)cols, (uint64_t)cols * 2, KCH,
+                 TN, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <bool GATEUP>
