@@ -68,75 +68,89 @@ __device__ __forceinline__ void load_inputs8(const __nv_bfloat16* p, bool, float
   }
 }
 
-// One warp converts superblock `sb` (256 consecutive inputs) of m rows of src
-// (row stride ld elements) into B fragments. Tokens m..4*nt-1 get zeros.
+// One warp converts token t of superblock `sb` (256 consecutive inputs starting
+// at `row`) into B fragments; `zero` writes the zeros of a padding token.
 template <typename T>
-__device__ void prep_superblock(const T* src, int64_t ld, int m, int nt, int sb, FragPtrs f, bool coherent) {
+__device__ __forceinline__ void prep_token(const T* row, bool coherent, bool zero, int t, int nt, int sb,
+                                           FragPtrs f) {
   const int lane = threadIdx.x & 31;
   const int sbk = lane >> 2;              // sub-block of this lane's 8 inputs
   const int tgp = sbk >> 1, p = sbk & 1;  // quad thread owning that sub-block and its nibble half
-  for (int t = 0; t < 4 * nt; ++t) {
-    float v[8];
-    if (t < m) {
-      load_inputs8(src + (int64_t)t * ld + (int64_t)sb * QK + lane * 8, coherent, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = warp_max(amax);
-    int e = 0;
-    if (amax > 0.f) e = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100);
-    const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-    __half hi[8], lo[8];
-    float xsum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float y = v[i] * s;
-      hi[i] = __float2half_rn(y);
-      lo[i] = __float2half_rn(y - __half2float(hi[i]));
-      xsum += y;
-    }
-    xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
-    xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
-    const int ntile = t >> 2, gbase = 2 * (t & 3);
+  const int ntile = t >> 2, gbase = 2 * (t & 3);
+  uint2* fx = f.fx + ((int64_t)sb * 16 * nt + ntile) * 32 + tgp;
+  uint32_t* fm = f.fm + ((int64_t)sb * nt + ntile) * 32 + (lane >> 3);
+  if (zero) {
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int w = (lane & 3) * 2 + hh;
-      const int step = 2 * w + p;
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const __half* h8 = part ? lo : hi;
-        uint2 fr;
-        fr.x = h2_as_u32(__halves2half2(h8[4 * hh + 0], h8[4 * hh + 2]));
-        fr.y = h2_as_u32(__halves2half2(h8[4 * hh + 1], h8[4 * hh + 3]));
-        f.fx[(((int64_t)sb * 16 + step) * nt + ntile) * 32 + (gbase + part) * 4 + tgp] = fr;
-      }
+      const int step = 2 * ((lane & 3) * 2 + hh) + p;
+      fx[(int64_t)step * nt * 32 + gbase * 4] = make_uint2(0u, 0u);
+      fx[(int64_t)step * nt * 32 + (gbase + 1) * 4] = make_uint2(0u, 0u);
     }
-    // X_j * 2^-6 keeps the sub-block sums inside the fp16 range
-    const float xl = __shfl_sync(0xffffffffu, xsum, lane & ~7) * 0.015625f;
-    const float xh = __shfl_sync(0xffffffffu, xsum, (lane & ~7) + 4) * 0.015625f;
-    if ((lane & 7) == 0) {
-      const __half xlh = __float2half_rn(xl), xhh = __float2half_rn(xh);
-      const __half xll = __float2half_rn(xl - __half2float(xlh)), xhl = __float2half_rn(xh - __half2float(xhh));
-      const int tq = lane >> 3;
-      f.fm[((int64_t)sb * nt + ntile) * 32 + (gbase + 0) * 4 + tq] = h2_as_u32(__halves2half2(xlh, xhh));
-      f.fm[((int64_t)sb * nt + ntile) * 32 + (gbase + 1) * 4 + tq] = h2_as_u32(__halves2half2(xll, xhl));
-    }
-    if (lane == 0) f.sc[(int64_t)sb * 8 + t] = __uint_as_float((uint32_t)(127 + e) << 23);
+    if ((lane & 7) == 0) fm[gbase * 4] = fm[(gbase + 1) * 4] = 0u;
+    if (lane == 0) f.sc[(int64_t)sb * 8 + t] = 1.f;
+    return;
   }
+  float v[8];
+  load_inputs8(row + lane * 8, coherent, v);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = warp_max(amax);
+  int e = 0;
+  if (amax > 0.f) e = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100);
+  const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  __half hi[8], lo[8];
+  float xsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = v[i] * s;
+    hi[i] = __float2half_rn(y);
+    lo[i] = __float2half_rn(y - __half2float(hi[i]));
+    xsum += y;
+  }
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int step = 2 * ((lane & 3) * 2 + hh) + p;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const __half* h8 = part ? lo : hi;
+      uint2 fr;
+      fr.x = h2_as_u32(__halves2half2(h8[4 * hh + 0], h8[4 * hh + 2]));
+      fr.y = h2_as_u32(__halves2half2(h8[4 * hh + 1], h8[4 * hh + 3]));
+      fx[(int64_t)step * nt * 32 + (gbase + part) * 4] = fr;
+    }
+  }
+  // X_j * 2^-6 keeps the sub-block sums inside the fp16 range
+  const float xl = __shfl_sync(0xffffffffu, xsum, lane & ~7) * 0.015625f;
+  const float xh = __shfl_sync(0xffffffffu, xsum, (lane & ~7) + 4) * 0.015625f;
+  if ((lane & 7) == 0) {
+    const __half xlh = __float2half_rn(xl), xhh = __float2half_rn(xh);
+    const __half xll = __float2half_rn(xl - __half2float(xlh)), xhl = __float2half_rn(xh - __half2float(xhh));
+    fm[gbase * 4] = h2_as_u32(__halves2half2(xlh, xhh));
+    fm[(gbase + 1) * 4] = h2_as_u32(__halves2half2(xll, xhl));
+  }
+  if (lane == 0) f.sc[(int64_t)sb * 8 + t] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
-// K0 also zeroes the split-K semaphores and h-block counters of this call; K1
-// and K2 touch them only after their dependent-launch wait on K0.
+// One warp converts all 4*nt token slots of superblock `sb` of src [m][ld].
+template <typename T>
+__device__ void prep_superblock(const T* src, int64_t ld, int m, int nt, int sb, FragPtrs f, bool coherent) {
+  for (int t = 0; t < 4 * nt; ++t)
+    prep_token<T>(src + (int64_t)min(t, m - 1) * ld + (int64_t)sb * QK, coherent, t >= m, t, nt, sb, f);
+}
+
+// K0: one CTA per superblock of x, one warp per token slot. It also zeroes the
+// split-K semaphores and h-block counters of this call; K1 and K2 touch them
+// only after their dependent-launch wait on K0.
 template <typename T>
 __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f,
                               uint32_t* __restrict__ counters, int ncounters) {
   pdl_launch_dependents();
-  for (int i = blockIdx.x * 32 + threadIdx.x; i < ncounters; i += gridDim.x * 32) counters[i] = 0u;
-  prep_superblock<T>(x, hidden, m, nt, blockIdx.x, f, false);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < ncounters; i += gridDim.x * blockDim.x) counters[i] = 0u;
+  const int t = threadIdx.x >> 5, sb = blockIdx.x;
+  prep_token<T>(x + (int64_t)min(t, m - 1) * hidden + (int64_t)sb * QK, false, t >= m, t, nt, sb, f);
 }
 
 struct GemvParams {
@@ -209,12 +223,17 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams P) {
   constexpr int ROWS = 16;
-  constexpr int MAT_BYTES = ROWS * BLK;  // one 16-row x 1-superblock tile
-  constexpr int STAGE_BYTES = NMAT * MAT_BYTES;
+  constexpr int TILE = ROWS * BLK;        // one 16-row x 1-superblock tile of one matrix
+  constexpr int STREAMS = WARPS / NMAT;   // units are walked by warp pairs (gate, up) when NMAT == 2
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
-  uint8_t* ring = smem + warp * STAGES * STAGE_BYTES;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * STAGE_BYTES) + warp * STAGES;
+  const int mat = (NMAT == 2) ? (warp & 1) : 0;
+  const int strm = (NMAT == 2) ? (warp >> 1) : warp;
+  uint8_t* ring = smem + warp * STAGES * TILE;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WARPS * STAGES * TILE) + warp * STAGES;
+  // gate/up exchange slots: [stream][2][32 lanes][NT][2]
+  float* xch = reinterpret_cast<float*>(smem + WARPS * STAGES * TILE + WARPS * STAGES * 8);
+  const CUtensorMap* tm = mat ? &tm1 : &tm0;
 
   const int nrt = P.rows / ROWS;
   const int64_t U = (int64_t)P.nks * nrt;
@@ -228,7 +247,7 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   __syncwarp();
 
   // issue cursor (which step the next tile load fetches)
-  int64_t iu = u0 + warp;
+  int64_t iu = u0 + strm;
   int isb = 0, isb_end = 0, irt = 0;
   if (iu < u1) {
     irt = (int)(iu % nrt);
@@ -240,13 +259,11 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      uint8_t* dst = ring + stage * STAGE_BYTES;
-      mbar_arrive_expect_tx(&bar[stage], STAGE_BYTES);
-      tma_tile(dst, &tm0, isb * (BLK / 8), irt * ROWS, &bar[stage], pol);
-      if (NMAT == 2) tma_tile(dst + MAT_BYTES, &tm1, isb * (BLK / 8), irt * ROWS, &bar[stage], pol);
+      mbar_arrive_expect_tx(&bar[stage], TILE);
+      tma_tile(ring + stage * TILE, tm, isb * (BLK / 8), irt * ROWS, &bar[stage], pol);
     }
     if (++isb == isb_end) {
-      iu += WARPS;
+      iu += STREAMS;
       if (iu < u1) {
         irt = (int)(iu % nrt);
         isb = (int)(iu / nrt) * P.kc;
@@ -260,25 +277,28 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   pdl_launch_dependents();
   pdl_wait();  // input fragments come from the previous kernel
 
-  const ScaleSel ssel{8u * 2u * (uint32_t)(tig & 1), tig >= 2};
+  const uint32_t sshift = 16u * (uint32_t)(tig & 1);  // byte pair of the owned sub-blocks
+  const bool shigh = tig >= 2;                       // owned sub-blocks are 4..7
+  bool live[NT];                                     // B lanes that hold a real token
+#pragma unroll
+  for (int n = 0; n < NT; ++n) live[n] = (lane >> 3) < P.m - 4 * n;
 
   // consume cursor
-  int64_t cu = u0 + warp;
-  int csb = 0, csb_end = 0, crt = 0, cks = 0;
+  int64_t cu = u0 + strm;
+  int csb = 0, csb_end = 0, crt = 0, cks = 0, nunit = 0;
   if (cu < u1) {
     crt = (int)(cu % nrt);
     cks = (int)(cu / nrt);
     csb = cks * P.kc;
     csb_end = min(P.nsb, csb + P.kc);
   }
-  float acc[NMAT][NT][2];
+  float acc[NT][2];
 #pragma unroll
-  for (int a = 0; a < NMAT; ++a)
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[a][n][0] = acc[a][n][1] = 0.f;
+  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
 
   int step = 0;
   bool failed = false;
+#pragma unroll 1
   while (cu < u1) {
     const int stage = step % STAGES;
     if (iu < u1) {
@@ -290,39 +310,38 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       break;
     }
     // ------------------------------------------------ one superblock of 16 rows
-    const uint8_t* st = ring + stage * STAGE_BYTES;
-    uint4 q0[NMAT][2], q1[NMAT][2];
-    uint32_t A_min[NMAT][2];
-    __half2 mlo[NMAT][2], alo[NMAT][2], mhi[NMAT][2], ahi[NMAT][2];
-    float dd[NMAT][2], dm[NMAT][2];
+    const uint8_t* st = ring + stage * TILE;
+    uint4 q0[2], q1[2];
+    uint32_t A_min[2];
+    __half2 mlo[2], alo[2], mhi[2], ahi[2];
+    float dd[2], dm[2];
 #pragma unroll
-    for (int a = 0; a < NMAT; ++a) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint8_t* rb = st + a * MAT_BYTES + (g + 8 * r) * BLK;
-        const uint4 hd = *reinterpret_cast<const uint4*>(rb);
-        q0[a][r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
-        q1[a][r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
-        const float2 dpair = __half22float2(u32_as_h2(hd.x));
-        dd[a][r] = dpair.x;
-        dm[a][r] = dpair.y;
-        uint32_t sa, sb, ma, mb;
-        owned_scales(ssel, hd.y, hd.z, hd.w, sa, sb, ma, mb);
-        mlo[a][r] = small_int_h2(sa);
-        alo[a][r] = __hmul2(mlo[a][r], u32_as_h2(0xE400E400u));  // * -1024
-        const __half2 shb = small_int_h2(sb);
-        mhi[a][r] = __hmul2(shb, u32_as_h2(0x2C002C00u));        // * 1/16
-        ahi[a][r] = __hmul2(shb, u32_as_h2(0xD400D400u));        // * -64
-        A_min[a][r] = h2_as_u32(small_int_pair_h2(ma, mb));
-      }
+    for (int r = 0; r < 2; ++r) {
+      const uint8_t* rb = st + (g + 8 * r) * BLK;
+      const uint4 hd = *reinterpret_cast<const uint4*>(rb);
+      q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
+      q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
+      const float2 dpair = __half22float2(u32_as_h2(hd.x));
+      dd[r] = dpair.x;
+      dm[r] = dpair.y;
+      // 6-bit scale and min of the two owned sub-blocks (2*tig, 2*tig+1)
+      const uint32_t w0 = hd.y >> sshift, w1 = hd.z >> sshift, w2 = hd.w >> sshift;
+      const uint32_t sa = shigh ? ((w2 & 15u) | ((w0 >> 2) & 0x30u)) : (w0 & 63u);
+      const uint32_t sb = shigh ? (((w2 >> 8) & 15u) | ((w0 >> 10) & 0x30u)) : ((w0 >> 8) & 63u);
+      const uint32_t ma = shigh ? (((w2 >> 4) & 15u) | ((w1 >> 2) & 0x30u)) : (w1 & 63u);
+      const uint32_t mb = shigh ? (((w2 >> 12) & 15u) | ((w1 >> 10) & 0x30u)) : ((w1 >> 8) & 63u);
+      mlo[r] = small_int_h2(sa);
+      alo[r] = __hmul2(mlo[r], u32_as_h2(0xE400E400u));  // * -1024
+      const __half2 shb = small_int_h2(sb);
+      mhi[r] = __hmul2(shb, u32_as_h2(0x2C002C00u));     // * 1/16
+      ahi[r] = __hmul2(shb, u32_as_h2(0xD400D400u));     // * -64
+      A_min[r] = h2_as_u32(small_int_pair_h2(ma, mb));
     }
-    float c[NMAT][NT][2][4], cm[NMAT][NT][4];
+    float c[NT][2][4], cm[NT][4];
 #pragma unroll
-    for (int a = 0; a < NMAT; ++a)
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) c[a][n][0][i] = c[a][n][1][i] = cm[a][n][i] = 0.f;
+      for (int i = 0; i < 4; ++i) c[n][0][i] = c[n][1][i] = cm[n][i] = 0.f;
 
     const uint2* fx = P.in.fx + (int64_t)csb * 16 * NT * 32 + lane;
 #pragma unroll
@@ -330,77 +349,75 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
       uint2 b0[NT], b1[NT];
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        b0[n] = fx[((2 * w) * NT + n) * 32];
-        b1[n] = fx[((2 * w + 1) * NT + n) * 32];
+        b0[n] = live[n] ? fx[((2 * w) * NT + n) * 32] : make_uint2(0u, 0u);
+        b1[n] = live[n] ? fx[((2 * w + 1) * NT + n) * 32] : make_uint2(0u, 0u);
+      }
+      uint32_t L0[2], L1[2], H0[2], H1[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint4& qq = (w < 4) ? q0[r] : q1[r];
+        const uint32_t wd = (w & 3) == 0 ? qq.x : (w & 3) == 1 ? qq.y : (w & 3) == 2 ? qq.z : qq.w;
+        const uint32_t t8 = wd >> 8;
+        L0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x000F000Fu, 0x64006400u)), mlo[r], alo[r]));
+        L1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x000F000Fu, 0x64006400u)), mlo[r], alo[r]));
+        H0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x00F000F0u, 0x64006400u)), mhi[r], ahi[r]));
+        H1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x00F000F0u, 0x64006400u)), mhi[r], ahi[r]));
       }
 #pragma unroll
-      for (int a = 0; a < NMAT; ++a) {
-        uint32_t L0[2], L1[2], H0[2], H1[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint4& qq = (w < 4) ? q0[a][r] : q1[a][r];
-          const uint32_t wd = (w & 3) == 0 ? qq.x : (w & 3) == 1 ? qq.y : (w & 3) == 2 ? qq.z : qq.w;
-          const uint32_t t8 = wd >> 8;
-          L0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x000F000Fu, 0x64006400u)), mlo[a][r], alo[a][r]));
-          L1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x000F000Fu, 0x64006400u)), mlo[a][r], alo[a][r]));
-          H0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x00F000F0u, 0x64006400u)), mhi[a][r], ahi[a][r]));
-          H1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x00F000F0u, 0x64006400u)), mhi[a][r], ahi[a][r]));
-        }
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          mma16816(c[a][n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
-          mma16816(c[a][n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
-        }
+      for (int n = 0; n < NT; ++n) {
+        mma16816(c[n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
+        mma16816(c[n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
       }
     }
     {
       const uint32_t* fm = P.in.fm + (int64_t)csb * NT * 32 + lane;
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const uint32_t bm = fm[n * 32];
-#pragma unroll
-        for (int a = 0; a < NMAT; ++a) mma16816(cm[a][n], A_min[a][0], A_min[a][1], 0u, 0u, bm, 0u);
+        const uint32_t bm = live[n] ? fm[n * 32] : 0u;
+        mma16816(cm[n], A_min[0], A_min[1], 0u, 0u, bm, 0u);
       }
     }
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
       const float xs = P.in.sc[(int64_t)csb * 8 + n * 4 + tig];
 #pragma unroll
-      for (int a = 0; a < NMAT; ++a) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float main = (c[a][n][0][2 * r] + c[a][n][1][2 * r]) + (c[a][n][0][2 * r + 1] + c[a][n][1][2 * r + 1]);
-          const float mins = cm[a][n][2 * r] + cm[a][n][2 * r + 1];
-          acc[a][n][r] = fmaf(main, dd[a][r] * xs, acc[a][n][r]);
-          acc[a][n][r] = fmaf(-mins, dm[a][r] * (64.f * xs), acc[a][n][r]);
-        }
+      for (int r = 0; r < 2; ++r) {
+        const float main = (c[n][0][2 * r] + c[n][1][2 * r]) + (c[n][0][2 * r + 1] + c[n][1][2 * r + 1]);
+        const float mins = cm[n][2 * r] + cm[n][2 * r + 1];
+        acc[n][r] = fmaf(main, dd[r] * xs, acc[n][r]);
+        acc[n][r] = fmaf(-mins, dm[r] * (64.f * xs), acc[n][r]);
       }
     }
     ++step;
     // ------------------------------------------------ end of a unit
     if (++csb == csb_end) {
       const int row0 = crt * ROWS;
-      bool last = true;
-      if (P.nks > 1) {
+      float fin[NMAT][NT][2];
+      bool owner = true;  // the warp that finishes the unit (gate warp of a pair)
+      if (NMAT == 2) {
+        float* slot = xch + (((strm * 2 + (nunit & 1)) * 32 + lane) * NT) * 2;
+        if (mat == 1) {
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const int tok = n * 4 + tig;
-          if (tok < P.m) {
+          for (int n = 0; n < NT; ++n) slot[2 * n] = acc[n][0], slot[2 * n + 1] = acc[n][1];
+        }
+        asm volatile("bar.sync %0, 64;" ::"r"(1 + strm) : "memory");
+        owner = (mat == 0);
+        if (owner) {
 #pragma unroll
-            for (int a = 0; a < NMAT; ++a)
-#pragma unroll
-              for (int r = 0; r < 2; ++r)
-                P.part[(((int64_t)cks * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r] = acc[a][n][r];
+          for (int n = 0; n < NT; ++n) {
+            fin[0][n][0] = acc[n][0];
+            fin[0][n][1] = acc[n][1];
+            fin[NMAT - 1][n][0] = slot[2 * n];
+            fin[NMAT - 1][n][1] = slot[2 * n + 1];
           }
         }
-        __threadfence();
-        __syncwarp();
-        uint32_t old = 0;
-        if (lane == 0) old = atomicAdd(&P.sem[crt], 1u);
-        old = __shfl_sync(0xffffffffu, old, 0);
-        last = (old == (uint32_t)(P.nks - 1));
-        if (last) {
-          __threadfence();
+      } else {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) fin[0][n][0] = acc[n][0], fin[0][n][1] = acc[n][1];
+      }
+      if (owner) {
+        bool last = true;
+        if (P.nks > 1) {
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
             const int tok = n * 4 + tig;
@@ -408,49 +425,68 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
 #pragma unroll
               for (int a = 0; a < NMAT; ++a)
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  float s = 0.f;
-                  for (int k = 0; k < P.nks; ++k)
-                    s += __ldcg(&P.part[(((int64_t)k * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r]);
-                  acc[a][n][r] = s;
-                }
+                for (int r = 0; r < 2; ++r)
+                  P.part[(((int64_t)cks * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r] = fin[a][n][r];
             }
           }
-          if (lane == 0) P.sem[crt] = 0u;
-        }
-      }
-      if (last) {
-#pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          const int tok = n * 4 + tig;
-          if (tok < P.m) {
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              const float v = (NMAT == 2) ? silu_f(acc[0][n][r]) * acc[NMAT - 1][n][r] : acc[0][n][r];
-              P.out[(int64_t)tok * P.rows + row0 + g + 8 * r] = v;
-            }
-          }
-        }
-        if (NMAT == 2) {
-          // the last of the 16 tiles of a 256-row block of h converts it for the down projection
           __threadfence();
           __syncwarp();
-          const int sbh = row0 / QK;
           uint32_t old = 0;
-          if (lane == 0) old = atomicAdd(&P.cnt_next[sbh], 1u);
+          if (lane == 0) old = atomicAdd(&P.sem[crt], 1u);
           old = __shfl_sync(0xffffffffu, old, 0);
-          if (old == (uint32_t)(QK / ROWS - 1)) {
+          last = (old == (uint32_t)(P.nks - 1));
+          if (last) {
             __threadfence();
-            prep_superblock<float>(P.out, P.rows, P.m, NT, sbh, P.next, true);
-            if (lane == 0) P.cnt_next[sbh] = 0u;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+              const int tok = n * 4 + tig;
+              if (tok < P.m) {
+#pragma unroll
+                for (int a = 0; a < NMAT; ++a)
+#pragma unroll
+                  for (int r = 0; r < 2; ++r) {
+                    float sum = 0.f;
+                    for (int k = 0; k < P.nks; ++k)
+                      sum += __ldcg(&P.part[(((int64_t)k * NMAT + a) * P.m + tok) * P.rows + row0 + g + 8 * r]);
+                    fin[a][n][r] = sum;
+                  }
+              }
+            }
+            if (lane == 0) P.sem[crt] = 0u;
+          }
+        }
+        if (last) {
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            const int tok = n * 4 + tig;
+            if (tok < P.m) {
+#pragma unroll
+              for (int r = 0; r < 2; ++r) {
+                const float v = (NMAT == 2) ? silu_f(fin[0][n][r]) * fin[NMAT - 1][n][r] : fin[0][n][r];
+                P.out[(int64_t)tok * P.rows + row0 + g + 8 * r] = v;
+              }
+            }
+          }
+          if (NMAT == 2) {
+            // the last of the 16 tiles of a 256-row block of h converts it for the down projection
+            __threadfence();
+            __syncwarp();
+            const int sbh = row0 / QK;
+            uint32_t old = 0;
+            if (lane == 0) old = atomicAdd(&P.cnt_next[sbh], 1u);
+            old = __shfl_sync(0xffffffffu, old, 0);
+            if (old == (uint32_t)(QK / ROWS - 1)) {
+              __threadfence();
+              prep_superblock<float>(P.out, P.rows, P.m, NT, sbh, P.next, true);
+              if (lane == 0) P.cnt_next[sbh] = 0u;
+            }
           }
         }
       }
 #pragma unroll
-      for (int a = 0; a < NMAT; ++a)
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[a][n][0] = acc[a][n][1] = 0.f;
-      cu += WARPS;
+      for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
+      ++nunit;
+      cu += STREAMS;
       if (cu < u1) {
         crt = (int)(cu % nrt);
         cks = (int)(cu / nrt);
@@ -465,15 +501,18 @@ __global__ void __launch_bounds__(WARPS * 32, 1)
   }
 }
 
-constexpr int WARPS = 8;
-constexpr int STAGES1 = 4;  // K1 stages per warp (2 x 16 rows x 144 B each)
-constexpr int STAGES2 = 6;  // K2 stages per warp (16 rows x 144 B each)
+// Warps per CTA and ring stages per warp: 16 warps for up to 4 tokens (128
+// registers per thread), 10 warps for 5-8 tokens, whose fragments need more.
+template <int NT> struct Shape;
+template <> struct Shape<1> { static constexpr int WARPS = 16, STAGES = 4; };
+template <> struct Shape<2> { static constexpr int WARPS = 10, STAGES = 6; };
 
-template <int NMAT, int NT, int STAGES>
+template <int NMAT, int NT>
 cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                         cudaStream_t s) {
-  auto kern = gemv_kernel<NMAT, NT, STAGES, WARPS>;
-  const size_t smem = (size_t)WARPS * STAGES * (NMAT * 16 * BLK + 8);
+  constexpr int W = Shape<NT>::WARPS, S = Shape<NT>::STAGES;
+  auto kern = gemv_kernel<NMAT, NT, S, W>;
+  const size_t smem = (size_t)W * S * (16 * BLK + 8) + (size_t)(W / NMAT) * 2 * 32 * NT * 2 * 4;
   static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -485,7 +524,7 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(WARPS * 32);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -503,22 +542,26 @@ bool weight_map(CUtensorMap* m, const void* w, int rows, int nsb) {
                  (uint64_t)nsb * BLK, BLK / 8, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Choose the number of K-splits: the fewest that keep the per-CTA unit counts
-// within ~7% of each other.
-void choose_split(int nsb, int nrt, int grid, int* nks_out, int* kc_out) {
-  double best_eff = -1;
+// Choose the number of K-splits. A CTA walks its contiguous range of units with
+// `streams` independent unit streams (warps, or warp pairs for gate/up); the
+// cost is the longest stream's superblock steps plus about one step of
+// split-K fixup per unit when K is split.
+void choose_split(int nsb, int nrt, int grid, int streams, int* nks_out, int* kc_out) {
+  double best = 1e30;
   int best_nks = 1, best_kc = nsb;
   for (int t = 1; t <= nsb; ++t) {
     const int kc = (nsb + t - 1) / t;
     const int nks = (nsb + kc - 1) / kc;
-    const double per = (double)nks * nrt / grid;
-    const double eff = per / std::ceil(per);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
+    if (nks != t) continue;
+    const int64_t units = (int64_t)nks * nrt;
+    const int64_t per_cta = (units + grid - 1) / grid;
+    const int64_t per_stream = (per_cta + streams - 1) / streams;
+    const double cost = (double)per_stream * kc + (nks > 1 ? (double)per_stream : 0.0);
+    if (cost < best - 1e-9) {
+      best = cost;
       best_nks = nks;
       best_kc = kc;
     }
-    if (eff >= 0.93) break;
   }
   *nks_out = best_nks;
   *kc_out = best_kc;
@@ -536,8 +579,9 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   p->nt = (int)((m + 3) / 4);
   const int nsb1 = (int)(hidden / QK), nsb2 = (int)(inter / QK);
   const int nrt1 = (int)(inter / 16), nrt2 = (int)(hidden / 16);
-  choose_split(nsb1, nrt1, num_sms, &p->nks1, &p->kc1);
-  choose_split(nsb2, nrt2, num_sms, &p->nks2, &p->kc2);
+  const int w = p->nt == 1 ? Shape<1>::WARPS : Shape<2>::WARPS;
+  choose_split(nsb1, nrt1, num_sms, w / 2, &p->nks1, &p->kc1);
+  choose_split(nsb2, nrt2, num_sms, w, &p->nks2, &p->kc2);
   p->grid1 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks1 * nrt1);
   p->grid2 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks2 * nrt2);
   size_t o = 0;
@@ -574,9 +618,9 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   prof.before(0, s);
   if (bf16)
     prep_x_kernel<__nv_bfloat16>
-        <<<nsb1, 32, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
+        <<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
   else
-    prep_x_kernel<float><<<nsb1, 32, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
+    prep_x_kernel<float><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1, counters, ncounters);
   prof.after(0, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -601,8 +645,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
       !weight_map(&md, wd, p.hidden, p.inter / QK))
     return cudaErrorInvalidValue;
   prof.before(1, s);
-  e = (p.nt == 1) ? launch_gemv<2, 1, STAGES1>(mg, mu, g1, p.grid1, s)
-                  : launch_gemv<2, 2, STAGES1>(mg, mu, g1, p.grid1, s);
+  e = (p.nt == 1) ? launch_gemv<2, 1>(mg, mu, g1, p.grid1, s) : launch_gemv<2, 2>(mg, mu, g1, p.grid1, s);
   prof.after(1, s);
   if (e != cudaSuccess) return e;
 
@@ -620,8 +663,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   g2.out = y;
   g2.err = err;
   prof.before(2, s);
-  e = (p.nt == 1) ? launch_gemv<1, 1, STAGES2>(md, md, g2, p.grid2, s)
-                  : launch_gemv<1, 2, STAGES2>(md, md, g2, p.grid2, s);
+  e = (p.nt == 1) ? launch_gemv<1, 1>(md, md, g2, p.grid2, s) : launch_gemv<1, 2>(md, md, g2, p.grid2, s);
   prof.after(2, s);
   return e;
 }
