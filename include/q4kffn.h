@@ -116,6 +116,27 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
                              const void* W_down, float* y, void* workspace, size_t ws_bytes,
                              q4k_stream_t stream);
 
+/* Decode-regime variant of ffn_q4k_swiglu (float32 x, m = 1..8, hidden and
+ * inter multiples of 256 up to 16384) that allocates no device memory, for
+ * callers that cannot call cudaMalloc: a serving process whose memory pool owns
+ * all device memory after start-up, or a latency-critical loop that cannot
+ * afford cudaMalloc's possible device-wide synchronisation. It has no
+ * counterpart on the source pages. Its scratch is a 16 MiB array inside the
+ * library image (a file-scope __device__ array that every GPU loading the
+ * library holds until the process exits), enough for every accepted shape; m
+ * outside 1..8 or a dimension above 16384 returns Q4K_ERR_SHAPE, and a shape
+ * whose scratch would still exceed 16 MiB (possible only on parts with other SM
+ * counts) returns Q4K_ERR_NOMEM, both without launching. The first call on a device resolves the
+ * array's device address (cudaGetSymbolAddress) and checks the architecture,
+ * so make that first call before any stream capture. Every call on a device
+ * shares the one array and each call re-initialises what it reads; calls that
+ * overlap on the GPU (different streams, no ordering) race on it and must not
+ * be issued. Device-side wait timeouts of this entry point are recorded in a
+ * separate static word that q4k_check_device_error does not read. */
+q4k_status ffn_q4k_swiglu_noalloc(const void* x, int64_t m, int64_t hidden, int64_t inter,
+                                  const void* W_gate, const void* W_up, const void* W_down,
+                                  float* y, q4k_stream_t stream);
+
 /* Workspace bytes ffn_q4k_swiglu_ex needs for this shape (0 for an invalid shape). */
 size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
 
