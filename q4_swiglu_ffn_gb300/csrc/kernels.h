@@ -23,13 +23,12 @@ cudaError_t launch_quantize_weights(const void* w, int bf16, int64_t rows, int64
 struct DecodePlan {
   int m, hidden, inter;
   int nt;              // n-tiles of 4 tokens (1 or 2)
-  int nks1, kc1;       // gate/up K-splits and superblocks per split
-  int nks2, kc2;       // down K-splits
+  int nks1, kc1;       // gate/up K-chunks and superblock groups per chunk
+  int nks2, kc2;       // down K-chunks and superblock groups per chunk
   int grid1, grid2;    // CTAs
   size_t ws_bytes;     // workspace bytes
-  // workspace offsets (bytes)
-  size_t off_fx1, off_fm1, off_sc1, off_fx2, off_fm2, off_sc2, off_h, off_p1, off_p2, off_sem1, off_cnt2,
-      off_sem2;
+  // workspace offsets (bytes): fragments of x and of h, gate/up and down chunk sums
+  size_t off_fx1, off_fm1, off_sc1, off_fx2, off_fm2, off_sc2, off_p1, off_p2;
 };
 bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p);
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,

@@ -204,6 +204,64 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
+// SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7).
+// xg holds, per tile row (0-63 gate, 64-127 up, same 64 inter indices), the
+// 128 token columns already multiplied by 2^e_t. Item i = (token i/2, Q8_1
+// block i%2 of 32 inter rows); each warp takes items ew, ew+8, ... four at a
+// time so the shuffle and division chains of independent items overlap.
+__device__ __forceinline__ void gateup_final(const uint8_t* smem, const MmqParams& P, int mt, int nt, int ew,
+                                             int lane, volatile int* abort_flag) {
+  if (*abort_flag) return;
+  const float* xg = reinterpret_cast<const float*>(smem);
+  constexpr int LD = TN + 1;
+  const int t0 = nt * TN;
+  for (int base = ew; base < 2 * TN; base += 32) {
+    float h[4];
+    int tt[4], qb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int item = base + 8 * k;
+      tt[k] = item >> 1;
+      qb[k] = item & 1;
+      const float g = xg[(qb[k] * 32 + lane) * LD + tt[k]];
+      const float u = xg[(64 + qb[k] * 32 + lane) * LD + tt[k]];
+      h[k] = silu_f(g) * u;
+    }
+    float amax[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) amax[k] = fabsf(h[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], o));
+    int qi[4], sum[4];
+    float dq[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const bool nz = amax[k] >= 0x1p-120f;  // below: zero block (127/amax would overflow)
+      dq[k] = nz ? __fdiv_rn(amax[k], 127.f) : 0.f;
+      const float inv = nz ? __fdiv_rn(127.f, amax[k]) : 0.f;
+      float rq = roundf(__fmul_rn(h[k], inv));
+      rq = fminf(fmaxf(rq, -127.f), 127.f);
+      qi[k] = (int)rq;
+      sum[k] = qi[k];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sum[k] += __shfl_xor_sync(0xffffffffu, sum[k], o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = t0 + tt[k];
+      if (t < P.m) {
+        const int irow = mt * 64 + qb[k] * 32 + lane;
+        P.hq_qs[(int64_t)t * P.ldo + irow] = (int8_t)qi[k];
+        if (lane == 0) P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq[k], __fmul_rn(dq[k], (float)sum[k]));
+      }
+    }
+  }
+}
+
 template <bool GATEUP>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     mmq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constant__ CUtensorMap tm_lo,
@@ -317,16 +375,18 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(sb + 1) * BLK) + i);
       }
       const uint4 hd = cur[0];
+      uint32_t scs[8], mns[8];  // all 6-bit scales and mins of this superblock
+#pragma unroll
+      for (int j = 0; j < 8; ++j) scale_min(hd.y, hd.z, hd.w, j, scs[j], mns[j]);
+#pragma unroll
       for (int c = 0; c < CH_PER_SB; ++c) {
         const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
-        if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) { ok = false; break; }
+        if (!ok || (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err))) { ok = false; break; }
         uint8_t* arow = arow_base + s * STAGE_BYTES;
         if (c < 4) {
-          uint32_t sl, ml, sh, mh;
-          scale_min(hd.y, hd.z, hd.w, 2 * c, sl, ml);
-          scale_min(hd.y, hd.z, hd.w, 2 * c + 1, sh, mh);
-          const __half2 mlo = __float2half2_rn((float)sl), alo = __float2half2_rn(-1024.f * (float)sl);
-          const __half2 mhi = __float2half2_rn((float)sh * 0.0625f), ahi = __float2half2_rn(-64.f * (float)sh);
+          const __half2 mlo = __float2half2_rn((float)scs[2 * c]), alo = __float2half2_rn(-1024.f * (float)scs[2 * c]);
+          const __half2 mhi = __float2half2_rn((float)scs[2 * c + 1] * 0.0625f),
+                        ahi = __float2half2_rn(-64.f * (float)scs[2 * c + 1]);
           const uint4 ga = cur[1 + 2 * c], gb = cur[2 + 2 * c];
           const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
@@ -346,17 +406,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             *reinterpret_cast<uint4*>(arow + (((uint32_t)(4 + p) ^ rsw) << 4)) = hi4;
           }
         } else {
-          uint32_t mm[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t sc_;
-            scale_min(hd.y, hd.z, hd.w, j, sc_, mm[j]);
-          }
           uint4 v;
-          v.x = h2_as_u32(__halves2half2(__uint2half_rn(mm[0]), __uint2half_rn(mm[1])));
-          v.y = h2_as_u32(__halves2half2(__uint2half_rn(mm[2]), __uint2half_rn(mm[3])));
-          v.z = h2_as_u32(__halves2half2(__uint2half_rn(mm[4]), __uint2half_rn(mm[5])));
-          v.w = h2_as_u32(__halves2half2(__uint2half_rn(mm[6]), __uint2half_rn(mm[7])));
+          v.x = h2_as_u32(__halves2half2(__uint2half_rn(mns[0]), __uint2half_rn(mns[1])));
+          v.y = h2_as_u32(__halves2half2(__uint2half_rn(mns[2]), __uint2half_rn(mns[3])));
+          v.z = h2_as_u32(__halves2half2(__uint2half_rn(mns[4]), __uint2half_rn(mns[5])));
+          v.w = h2_as_u32(__halves2half2(__uint2half_rn(mns[6]), __uint2half_rn(mns[7])));
           *reinterpret_cast<uint4*>(arow + ((0u ^ rsw) << 4)) = v;
           *reinterpret_cast<uint4*>(arow + ((1u ^ rsw) << 4)) = v;
         }
@@ -364,6 +418,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[s]);
       }
+    }
+    if (GATEUP) {
+      // join the epilogue warps for the SwiGLU + Q8_1 pass over the finished tile
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      gateup_final(smem, P, mt, nt, warp - W_XF, lane, abort_flag);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -412,31 +471,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           const float sc = t < P.m ? P.tscale[t] : 0.f;
           xg[r * LD + i] = acc[i] * sc;
         }
+      } else {
+        *abort_flag = 1;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      if (ok && !*abort_flag) {
-        const int ew = warp - W_EPI;          // 0..3
-        const int qb = ew & 1;                // Q8_1 block: inter rows 32*qb .. +31 of the tile
-        const int tbeg = (ew >> 1) * (TN / 2);
-        const int irow = mt * 64 + qb * 32 + lane;
-        for (int i = tbeg; i < tbeg + TN / 2; ++i) {
-          const int t = t0 + i;
-          if (t >= P.m) break;
-          const float g = xg[(qb * 32 + lane) * LD + i], u = xg[(64 + qb * 32 + lane) * LD + i];
-          const float h = silu_f(g) * u;
-          const float amax = warp_max(fabsf(h));
-          const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
-          const float dq = nz ? __fdiv_rn(amax, 127.f) : 0.f;
-          const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
-          float rq = roundf(__fmul_rn(h, inv));
-          rq = fminf(fmaxf(rq, -127.f), 127.f);
-          int qi = (int)rq, sum = qi;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-          P.hq_qs[(int64_t)t * P.ldo + irow] = (int8_t)qi;
-          if (lane == 0) P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq, __fmul_rn(dq, (float)sum));
-        }
-      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      gateup_final(smem, P, mt, nt, 4 + (warp - W_EPI), lane, abort_flag);
     } else if (ok) {
       const int row = mt * TM + r;
 #pragma unroll
