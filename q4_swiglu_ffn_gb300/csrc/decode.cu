@@ -203,14 +203,6 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// half2(v, v) for an integer 0 <= v < 1024, exactly: (1024 + v) - 1024 in fp16
-__device__ __forceinline__ __half2 small_int_h2(uint32_t v) {
-  return __hsub2(u32_as_h2(0x64006400u | (v * 0x00010001u)), u32_as_h2(0x64006400u));
-}
-__device__ __forceinline__ __half2 small_int_pair_h2(uint32_t a, uint32_t b) {
-  return __hsub2(u32_as_h2(0x64006400u | a | (b << 16)), u32_as_h2(0x64006400u));
-}
-
 // 3-D box {18 x 8-byte elements of a block, rows, superblocks} of a weight matrix.
 __device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* tm, int row, int sb, uint64_t* bar,
                                          uint64_t policy) {
@@ -286,12 +278,24 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   pdl_launch_dependents();
   pdl_wait();  // input fragments come from the previous kernel
 
-  bool live[NT];  // B lanes that hold a real token
+  // B fragment lane to read for token tile n: this lane when its token is real,
+  // else the same position of token 4n (always real); the columns of padding
+  // tokens then hold copies that are never stored.
+  int flane[NT];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) live[n] = (lane >> 3) < P.m - 4 * n;
-  // byte pair of the two sub-blocks this thread owns (2*tig, 2*tig+1) in the scale field
-  const uint32_t sshift = 16u * (uint32_t)(tig & 1);
+  for (int n = 0; n < NT; ++n) flane[n] = ((lane >> 3) < P.m - 4 * n) ? lane : (lane & 7);
+  // Sub-blocks 2*tig and 2*tig+1 of a row are this thread's. Their 6-bit scales
+  // and mins are gathered from the 12-byte field with byte permutes whose
+  // selectors and masks depend only on tig: for sub-blocks 0-3 a scale (min) is
+  // the low 6 bits of byte j (j+4); for 4-7 it is the low (high) nibble of
+  // byte j+4 with the top two bits of byte j-4 (j) above it.
+  const uint32_t bb = 2u * (uint32_t)(tig & 1);
   const bool shigh = tig >= 2;
+  const uint32_t selS0 = shigh ? ((4u + bb) | bb << 4 | (4u + bb) << 8 | bb << 12) : bb * 0x1111u;
+  const uint32_t selS1 = selS0 + 0x1111u;
+  const uint32_t selM = shigh ? ((4u + bb) | bb << 4 | (5u + bb) << 8 | (bb + 1u) << 12)
+                              : (bb | bb << 4 | (bb + 1u) << 8 | (bb + 1u) << 12);
+  const uint32_t mL = shigh ? 0x000F000Fu : 0x003F003Fu, mH = shigh ? 0x00300030u : 0u, sM = shigh ? 4u : 0u;
 
   // ---------------------------------------------------------------- consumer (all warps)
   int64_t cu = u0;
@@ -328,31 +332,30 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
         const float2 dpair = __half22float2(u32_as_h2(hd.x));
         dd[r] = dpair.x;
         dm[r] = dpair.y;
-        const uint32_t w0 = hd.y >> sshift, w1 = hd.z >> sshift, w2 = hd.w >> sshift;
-        const uint32_t sa = shigh ? ((w2 & 15u) | ((w0 >> 2) & 0x30u)) : (w0 & 63u);
-        const uint32_t sb2 = shigh ? (((w2 >> 8) & 15u) | ((w0 >> 10) & 0x30u)) : ((w0 >> 8) & 63u);
-        const uint32_t ma = shigh ? (((w2 >> 4) & 15u) | ((w1 >> 2) & 0x30u)) : (w1 & 63u);
-        const uint32_t mb = shigh ? (((w2 >> 12) & 15u) | ((w1 >> 10) & 0x30u)) : ((w1 >> 8) & 63u);
-        mlo[r] = small_int_h2(sa);
-        alo[r] = __hmul2(mlo[r], u32_as_h2(0xE400E400u));  // * -1024
-        const __half2 shb = small_int_h2(sb2);
-        mhi[r] = __hmul2(shb, u32_as_h2(0x2C002C00u));     // * 1/16
-        ahi[r] = __hmul2(shb, u32_as_h2(0xD400D400u));     // * -64
-        A_min[r] = h2_as_u32(small_int_pair_h2(ma, mb));
+        // 0x6400 | value in each half: fp16 1024 + value
+        const uint32_t p0 = prmt(hd.y, hd.w, selS0), p1 = prmt(hd.y, hd.w, selS1), pm = prmt(hd.z, hd.w, selM);
+        const uint32_t s0b = lop3_and_or(p0, mL, lop3_and_or(p0 >> 10, mH, 0x64006400u));
+        const uint32_t s1b = lop3_and_or(p1, mL, lop3_and_or(p1 >> 10, mH, 0x64006400u));
+        const uint32_t mnb = lop3_and_or(pm >> sM, mL, lop3_and_or(pm >> 10, mH, 0x64006400u));
+        mlo[r] = __hsub2(u32_as_h2(s0b), u32_as_h2(0x64006400u));                      // scale, scale
+        alo[r] = __hmul2(mlo[r], u32_as_h2(0xE400E400u));                              // * -1024
+        mhi[r] = __hfma2(u32_as_h2(s1b), u32_as_h2(0x2C002C00u), u32_as_h2(0xD400D400u));  // scale / 16
+        ahi[r] = __hmul2(mhi[r], u32_as_h2(0xE400E400u));                              // -64 * scale
+        A_min[r] = h2_as_u32(__hsub2(u32_as_h2(mnb), u32_as_h2(0x64006400u)));
       }
       float c[NT][2][4], cm[NT][4];
 #pragma unroll
       for (int n = 0; n < NT; ++n)
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[n][0][i] = c[n][1][i] = cm[n][i] = 0.f;
-      const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32 + lane;
+      const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         uint2 b0[NT], b1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          b0[n] = live[n] ? fx[((2 * w) * NT + n) * 32] : make_uint2(0u, 0u);
-          b1[n] = live[n] ? fx[((2 * w + 1) * NT + n) * 32] : make_uint2(0u, 0u);
+          b0[n] = fx[((2 * w) * NT + n) * 32 + flane[n]];
+          b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
         }
         uint32_t L0[2], L1[2], H0[2], H1[2];
 #pragma unroll
@@ -372,10 +375,10 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
         }
       }
       {
-        const uint32_t* fm = P.in.fm + (int64_t)sb * NT * 32 + lane;
+        const uint32_t* fm = P.in.fm + (int64_t)sb * NT * 32;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const uint32_t bm = live[n] ? fm[n * 32] : 0u;
+          const uint32_t bm = fm[n * 32 + flane[n]];
           mma16816(cm[n], A_min[0], A_min[1], 0u, 0u, bm, 0u);
         }
       }
