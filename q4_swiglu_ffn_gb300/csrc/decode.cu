@@ -307,6 +307,14 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   float acc[NT][2];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
+  // With up to 4 tokens a warp keeps the B fragments of its superblock in
+  // registers for as long as that superblock stays the same (with one group per
+  // K-chunk: until its chunk changes).
+  constexpr bool CACHE_B = NT == 1;
+  uint2 bc[CACHE_B ? 16 : 1];
+  uint32_t bmc = 0;
+  float xsc = 0.f;
+  int csb = -1;
 
 #pragma unroll 1
   while (cu < u1 && !failed) {
@@ -349,13 +357,25 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) c[n][0][i] = c[n][1][i] = cm[n][i] = 0.f;
       const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
+      if (CACHE_B && sb != csb) {
+#pragma unroll
+        for (int k = 0; k < (CACHE_B ? 16 : 1); ++k) bc[k] = fx[k * 32 + flane[0]];
+        bmc = P.in.fm[(int64_t)sb * 32 + flane[0]];
+        xsc = P.in.sc[(int64_t)sb * 8 + tig];
+        csb = sb;
+      }
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         uint2 b0[NT], b1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          b0[n] = fx[((2 * w) * NT + n) * 32 + flane[n]];
-          b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
+          if (CACHE_B) {
+            b0[n] = bc[(2 * w) % (CACHE_B ? 16 : 1)];
+            b1[n] = bc[(2 * w + 1) % (CACHE_B ? 16 : 1)];
+          } else {
+            b0[n] = fx[((2 * w) * NT + n) * 32 + flane[n]];
+            b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
+          }
         }
         uint32_t L0[2], L1[2], H0[2], H1[2];
 #pragma unroll
@@ -378,13 +398,13 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
         const uint32_t* fm = P.in.fm + (int64_t)sb * NT * 32;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const uint32_t bm = fm[n * 32 + flane[n]];
+          const uint32_t bm = CACHE_B ? bmc : fm[n * 32 + flane[n]];
           mma16816(cm[n], A_min[0], A_min[1], 0u, 0u, bm, 0u);
         }
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float xs = P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
+        const float xs = CACHE_B ? xsc : P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float main = (c[n][0][2 * r] + c[n][1][2 * r]) + (c[n][0][2 * r + 1] + c[n][1][2 * r + 1]);
@@ -509,7 +529,7 @@ bool weight_map(CUtensorMap* m, const void* w, int rows, int nsb, int box_rows, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Number of K-chunks: the fewest, up to max_nks, that minimise the longest CTA's
+// Number of K-chunks: the most, up to max_nks, among those that minimise the longest CTA's
 // group steps. The cap bounds the partial-sum buffers (nks x m x rows floats).
 void choose_split(int ngroups, int nru, int grid, int max_nks, int* nks_out, int* gpc_out) {
   int64_t best = INT64_MAX;
@@ -520,7 +540,7 @@ void choose_split(int ngroups, int nru, int grid, int max_nks, int* nks_out, int
     if (nks != t) continue;
     const int64_t per_cta = ((int64_t)nks * nru + grid - 1) / grid;
     const int64_t cost = per_cta * gpc;
-    if (cost < best) {
+    if (cost <= best) {  // ties go to more chunks: one group per chunk lets warps keep their inputs
       best = cost;
       best_nks = nks;
       best_gpc = gpc;
