@@ -227,54 +227,73 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
   float* red = reinterpret_cast<float*>(empty + STAGES);  // [2][WARPS][32 lanes][NT][2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * WARPS * 32 * NT * 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   const int combo = warp % COMBOS, slice = warp / COMBOS;
   const int nru = P.rows / RU;
   const int ngroups = (P.nsb + SLICES - 1) / SLICES;
-  const int64_t U = (int64_t)P.nks * nru;
-  const int64_t u0 = U * blockIdx.x / gridDim.x, u1 = U * (blockIdx.x + 1) / gridDim.x;
+  const int U = P.nks * nru;  // at most 16 chunks x 2^16 row units
+  const int u0 = (int)((int64_t)U * blockIdx.x / gridDim.x), u1 = (int)((int64_t)U * (blockIdx.x + 1) / gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], WARPS);
     }
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- producer (warp 0, lane 0)
   const bool producer = (warp == 0 && lane == 0);
-  int64_t pu = u0;
-  int pg = 0, pg_end = 0, pru = 0, pstep = 0;
-  auto unit_groups = [&](int64_t u, int& ru, int& gb, int& ge) {
-    const int ks = (int)(u / nru);
-    ru = (int)(u % nru);
-    gb = ks * P.gpc;
-    ge = min(ngroups, gb + P.gpc);
+  // Unit u = ks * nru + ru: K-chunk ks, row unit ru, superblock groups [g, ge).
+  // One division places a walk at its first unit; later units follow by counting.
+  struct Walk {
+    int u, ks, ru, g, ge;
   };
-  if (pu < u1) unit_groups(pu, pru, pg, pg_end);
+  auto walk_start = [&](Walk& w, int u) {
+    w.u = u;
+    w.ks = u / nru;
+    w.ru = u - w.ks * nru;
+    w.g = w.ks * P.gpc;
+    w.ge = min(ngroups, w.g + P.gpc);
+  };
+  auto walk_next = [&](Walk& w) {
+    ++w.u;
+    if (++w.ru == nru) {
+      w.ru = 0;
+      ++w.ks;
+    }
+    w.g = w.ks * P.gpc;
+    w.ge = min(ngroups, w.g + P.gpc);
+  };
+  Walk pw;
+  walk_start(pw, u0);
+  int pstep = 0;
   const uint64_t pol = policy_evict_first();
   auto produce = [&]() -> bool {  // issue the next step's loads; false on a timed-out wait
     const int s = pstep % STAGES;
     if (pstep >= STAGES && !mbar_wait(&empty[s], (uint32_t)((pstep / STAGES) - 1) & 1u, P.err)) return false;
     uint8_t* st = smem + s * STAGE_BYTES;
     mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
-    tma_box3(st, &tm0, pru * RU, pg * SLICES, &full[s], pol);
-    if (GATEUP) tma_box3(st + BOX_BYTES, &tm1, pru * RU, pg * SLICES, &full[s], pol);
+    tma_box3(st, &tm0, pw.ru * RU, pw.g * SLICES, &full[s], pol);
+    if (GATEUP) tma_box3(st + BOX_BYTES, &tm1, pw.ru * RU, pw.g * SLICES, &full[s], pol);
     ++pstep;
-    if (++pg == pg_end) {
-      ++pu;
-      if (pu < u1) unit_groups(pu, pru, pg, pg_end);
-    }
+    if (++pw.g == pw.ge) walk_next(pw);
     return true;
   };
-  bool failed = false;
+  bool failed = false;  // warp-uniform once the loop starts
   if (producer) {
-    for (int i = 0; i < STAGES - 1 && pu < u1; ++i)
-      if (!produce()) { failed = true; break; }
+    for (int i = 0; i < STAGES - 1 && pw.u < u1; ++i)
+      if (!produce()) {
+        failed = true;
+        *abort_flag = 1;
+        break;
+      }
   }
+  failed = __any_sync(0xffffffffu, failed);
   pdl_launch_dependents();
   pdl_wait();  // input fragments come from the previous kernel
 
@@ -298,12 +317,9 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   const uint32_t mL = shigh ? 0x000F000Fu : 0x003F003Fu, mH = shigh ? 0x00300030u : 0u, sM = shigh ? 4u : 0u;
 
   // ---------------------------------------------------------------- consumer (all warps)
-  int64_t cu = u0;
-  int cg = 0, cg_end = 0, cru = 0, cks = 0, nunit = 0, cstep = 0;
-  if (cu < u1) {
-    unit_groups(cu, cru, cg, cg_end);
-    cks = (int)(cu / nru);
-  }
+  Walk cw;
+  walk_start(cw, u0);
+  int nunit = 0, cstep = 0;
   float acc[NT][2];
 #pragma unroll
   for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
@@ -316,14 +332,30 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   float xsc = 0.f;
   int csb = -1;
 
+  // A warp whose wait timed out raises the CTA's abort flag and stops waiting,
+  // copying and computing, but still walks its units so that every warp reaches
+  // every unit-end barrier.
 #pragma unroll 1
-  while (cu < u1 && !failed) {
-    if (producer && pu < u1 && !produce()) { failed = true; break; }
+  while (cw.u < u1) {
+    bool pf = false;
+    if (producer && !failed && pw.u < u1) pf = !produce();
+    if (__any_sync(0xffffffffu, pf)) {
+      failed = true;
+      *abort_flag = 1;
+    }
     const int s = cstep % STAGES;
-    if (!mbar_wait(&full[s], (uint32_t)(cstep / STAGES) & 1u, P.err)) { failed = true; break; }
-    const int sb = cg * SLICES + slice;
-    const int chunk_end = min(P.nsb, (cks + 1) * P.gpc * SLICES);
-    if (sb < chunk_end) {
+    if (!failed) {
+      if (*abort_flag) {
+        failed = true;
+      } else {
+        const bool ok = mbar_wait(&full[s], (uint32_t)(cstep / STAGES) & 1u, P.err);
+        if (__any_sync(0xffffffffu, !ok)) failed = true;
+      }
+      if (failed) *abort_flag = 1;
+    }
+    const int sb = cw.g * SLICES + slice;
+    const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
+    if (!failed && sb < chunk_end) {
       // ------------------------------------------ one 16-row tile of one superblock
       const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? combo * BOX_BYTES + slice * RU * BLK
                                                                : (slice * RU + combo * ROWS) * BLK);
@@ -415,18 +447,18 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);
+    if (lane == 0 && !failed) mbar_arrive(&empty[s]);
     ++cstep;
     // ------------------------------------------------ end of a unit
-    if (++cg == cg_end) {
+    if (++cw.g == cw.ge) {
       float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * 32 * NT * 2 + lane * NT * 2;
 #pragma unroll
       for (int n = 0; n < NT; ++n) slot[2 * n] = acc[n][0], slot[2 * n + 1] = acc[n][1];
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
-      if (warp == 1 + (nunit % (WARPS - 1))) {
+      if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
         // owner: sum the SLICES partial dot products of every tile and store this chunk's sums
         const float* rs = red + (size_t)(nunit & 1) * WARPS * 32 * NT * 2 + lane * NT * 2;
-        const int row0 = cru * RU;
+        const int row0 = cw.ru * RU;
 #pragma unroll
         for (int cb = 0; cb < COMBOS; ++cb)
 #pragma unroll
@@ -440,8 +472,8 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
             }
             const int tok = n * 4 + tig;
             if (tok < P.m) {
-              float* o = GATEUP ? P.out + (((int64_t)cks * 2 + cb) * P.m + tok) * P.rows + row0
-                                : P.out + ((int64_t)cks * P.m + tok) * P.rows + row0 + ROWS * cb;
+              float* o = GATEUP ? P.out + (((int64_t)cw.ks * 2 + cb) * P.m + tok) * P.rows + row0
+                                : P.out + ((int64_t)cw.ks * P.m + tok) * P.rows + row0 + ROWS * cb;
               o[g] = s0;
               o[g + 8] = s1;
             }
@@ -450,16 +482,12 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
 #pragma unroll
       for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
       ++nunit;
-      ++cu;
-      if (cu < u1) {
-        unit_groups(cu, cru, cg, cg_end);
-        cks = (int)(cu / nru);
-      }
+      walk_next(cw);
     }
   }
-  if (failed && producer) {
+  if (producer && *abort_flag) {
     // let copies already in flight land before the CTA's shared memory goes away
-    for (int t = cstep; t < pstep; ++t)
+    for (int t = max(0, pstep - STAGES); t < pstep; ++t)
       (void)mbar_wait(&full[t % STAGES], (uint32_t)(t / STAGES) & 1u, nullptr);
   }
 }
@@ -477,7 +505,7 @@ template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
   using S = Shape<GATEUP, NT>;
   return (size_t)S::STAGES * S::COMBOS * 16 * S::SLICES * BLK + 2 * S::STAGES * 8 +
-         (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4;
+         (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
 }
 
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
