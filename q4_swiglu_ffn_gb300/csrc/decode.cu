@@ -213,11 +213,16 @@ __device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* tm, int r
       : "memory");
 }
 
-template <bool GATEUP, int NT, int COMBOS, int SLICES, int STAGES>
-__global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
+// COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
+// COMBOS consecutive tiles of W_down); each warp takes TPW of them (sharing the
+// B operand) at one of the SLICES superblocks.
+template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES>
+__global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, 1)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams P) {
-  constexpr int WARPS = COMBOS * SLICES;
+  constexpr int TG = COMBOS / TPW;  // tile groups
+  constexpr int WARPS = TG * SLICES;
+  static_assert(COMBOS % TPW == 0, "tiles split evenly over warps");
   constexpr int ROWS = 16;
   constexpr int RU = GATEUP ? ROWS : ROWS * COMBOS;    // output rows of a unit (per matrix)
   constexpr int MATS = GATEUP ? 2 : 1;
@@ -226,11 +231,11 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
   uint64_t* empty = full + STAGES;
-  float* red = reinterpret_cast<float*>(empty + STAGES);  // [2][WARPS][32 lanes][NT][2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * WARPS * 32 * NT * 2);
+  float* red = reinterpret_cast<float*>(empty + STAGES);  // [2][WARPS][32 lanes][TPW][NT][2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * WARPS * 32 * TPW * NT * 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
-  const int combo = warp % COMBOS, slice = warp / COMBOS;
+  const int tgrp = warp % TG, slice = warp / TG;
   const int nru = P.rows / RU;
   const int ngroups = (P.nsb + SLICES - 1) / SLICES;
   const int U = P.nks * nru;  // at most 16 chunks x 2^16 row units
@@ -320,9 +325,11 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   Walk cw;
   walk_start(cw, u0);
   int nunit = 0, cstep = 0;
-  float acc[NT][2];
+  float acc[TPW][NT][2];
 #pragma unroll
-  for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
+  for (int t = 0; t < TPW; ++t)
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = 0.f;
   // With up to 4 tokens a warp keeps the B fragments of its superblock in
   // registers for as long as that superblock stays the same (with one group per
   // K-chunk: until its chunk changes).
@@ -356,38 +363,44 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
     const int sb = cw.g * SLICES + slice;
     const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
     if (!failed && sb < chunk_end) {
-      // ------------------------------------------ one 16-row tile of one superblock
-      const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? combo * BOX_BYTES + slice * RU * BLK
-                                                               : (slice * RU + combo * ROWS) * BLK);
-      uint4 q0[2], q1[2];
-      uint32_t A_min[2];
-      __half2 mlo[2], alo[2], mhi[2], ahi[2];
-      float dd[2], dm[2];
+      // ------------------------------------------ TPW 16-row tiles of one superblock
+      uint4 q0[TPW][2], q1[TPW][2];
+      uint32_t A_min[TPW][2];
+      __half2 mlo[TPW][2], alo[TPW][2], mhi[TPW][2], ahi[TPW][2];
+      float dd[TPW][2], dm[TPW][2];
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint8_t* rb = base + (g + 8 * r) * BLK;
-        const uint4 hd = *reinterpret_cast<const uint4*>(rb);
-        q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
-        q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
-        const float2 dpair = __half22float2(u32_as_h2(hd.x));
-        dd[r] = dpair.x;
-        dm[r] = dpair.y;
-        // 0x6400 | value in each half: fp16 1024 + value
-        const uint32_t p0 = prmt(hd.y, hd.w, selS0), p1 = prmt(hd.y, hd.w, selS1), pm = prmt(hd.z, hd.w, selM);
-        const uint32_t s0b = lop3_and_or(p0, mL, lop3_and_or(p0 >> 10, mH, 0x64006400u));
-        const uint32_t s1b = lop3_and_or(p1, mL, lop3_and_or(p1 >> 10, mH, 0x64006400u));
-        const uint32_t mnb = lop3_and_or(pm >> sM, mL, lop3_and_or(pm >> 10, mH, 0x64006400u));
-        mlo[r] = __hsub2(u32_as_h2(s0b), u32_as_h2(0x64006400u));                      // scale, scale
-        alo[r] = __hmul2(mlo[r], u32_as_h2(0xE400E400u));                              // * -1024
-        mhi[r] = __hfma2(u32_as_h2(s1b), u32_as_h2(0x2C002C00u), u32_as_h2(0xD400D400u));  // scale / 16
-        ahi[r] = __hmul2(mhi[r], u32_as_h2(0xE400E400u));                              // -64 * scale
-        A_min[r] = h2_as_u32(__hsub2(u32_as_h2(mnb), u32_as_h2(0x64006400u)));
+      for (int t = 0; t < TPW; ++t) {
+        const int cb = tgrp * TPW + t;
+        const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
+                                                                 : (slice * RU + cb * ROWS) * BLK);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint8_t* rb = base + (g + 8 * r) * BLK;
+          const uint4 hd = *reinterpret_cast<const uint4*>(rb);
+          q0[t][r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
+          q1[t][r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
+          const float2 dpair = __half22float2(u32_as_h2(hd.x));
+          dd[t][r] = dpair.x;
+          dm[t][r] = dpair.y;
+          // 0x6400 | value in each half: fp16 1024 + value
+          const uint32_t p0 = prmt(hd.y, hd.w, selS0), p1 = prmt(hd.y, hd.w, selS1), pm = prmt(hd.z, hd.w, selM);
+          const uint32_t s0b = lop3_and_or(p0, mL, lop3_and_or(p0 >> 10, mH, 0x64006400u));
+          const uint32_t s1b = lop3_and_or(p1, mL, lop3_and_or(p1 >> 10, mH, 0x64006400u));
+          const uint32_t mnb = lop3_and_or(pm >> sM, mL, lop3_and_or(pm >> 10, mH, 0x64006400u));
+          mlo[t][r] = __hsub2(u32_as_h2(s0b), u32_as_h2(0x64006400u));                        // scale, scale
+          alo[t][r] = __hmul2(mlo[t][r], u32_as_h2(0xE400E400u));                             // * -1024
+          mhi[t][r] = __hfma2(u32_as_h2(s1b), u32_as_h2(0x2C002C00u), u32_as_h2(0xD400D400u));  // scale / 16
+          ahi[t][r] = __hmul2(mhi[t][r], u32_as_h2(0xE400E400u));                             // -64 * scale
+          A_min[t][r] = h2_as_u32(__hsub2(u32_as_h2(mnb), u32_as_h2(0x64006400u)));
+        }
       }
-      float c[NT][2][4], cm[NT][4];
+      float c[TPW][NT][2][4], cm[TPW][NT][4];
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
+      for (int t = 0; t < TPW; ++t)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) c[n][0][i] = c[n][1][i] = cm[n][i] = 0.f;
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c[t][n][0][i] = c[t][n][1][i] = cm[t][n][i] = 0.f;
       const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
       if (CACHE_B && sb != csb) {
 #pragma unroll
@@ -409,21 +422,24 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
             b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
           }
         }
-        uint32_t L0[2], L1[2], H0[2], H1[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const uint4& qq = (w < 4) ? q0[r] : q1[r];
-          const uint32_t wd = (w & 3) == 0 ? qq.x : (w & 3) == 1 ? qq.y : (w & 3) == 2 ? qq.z : qq.w;
-          const uint32_t t8 = wd >> 8;
-          L0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x000F000Fu, 0x64006400u)), mlo[r], alo[r]));
-          L1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x000F000Fu, 0x64006400u)), mlo[r], alo[r]));
-          H0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x00F000F0u, 0x64006400u)), mhi[r], ahi[r]));
-          H1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x00F000F0u, 0x64006400u)), mhi[r], ahi[r]));
-        }
+        for (int t = 0; t < TPW; ++t) {
+          uint32_t L0[2], L1[2], H0[2], H1[2];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) {
-          mma16816(c[n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
-          mma16816(c[n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
+          for (int r = 0; r < 2; ++r) {
+            const uint4& qq = (w < 4) ? q0[t][r] : q1[t][r];
+            const uint32_t wd = (w & 3) == 0 ? qq.x : (w & 3) == 1 ? qq.y : (w & 3) == 2 ? qq.z : qq.w;
+            const uint32_t t8 = wd >> 8;
+            L0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x000F000Fu, 0x64006400u)), mlo[t][r], alo[t][r]));
+            L1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x000F000Fu, 0x64006400u)), mlo[t][r], alo[t][r]));
+            H0[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(wd, 0x00F000F0u, 0x64006400u)), mhi[t][r], ahi[t][r]));
+            H1[r] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t8, 0x00F000F0u, 0x64006400u)), mhi[t][r], ahi[t][r]));
+          }
+#pragma unroll
+          for (int n = 0; n < NT; ++n) {
+            mma16816(c[t][n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
+            mma16816(c[t][n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
+          }
         }
       }
       {
@@ -431,19 +447,23 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           const uint32_t bm = CACHE_B ? bmc : fm[n * 32 + flane[n]];
-          mma16816(cm[n], A_min[0], A_min[1], 0u, 0u, bm, 0u);
+#pragma unroll
+          for (int t = 0; t < TPW; ++t) mma16816(cm[t][n], A_min[t][0], A_min[t][1], 0u, 0u, bm, 0u);
         }
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
         const float xs = CACHE_B ? xsc : P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const float main = (c[n][0][2 * r] + c[n][1][2 * r]) + (c[n][0][2 * r + 1] + c[n][1][2 * r + 1]);
-          const float mins = cm[n][2 * r] + cm[n][2 * r + 1];
-          acc[n][r] = fmaf(main, dd[r] * xs, acc[n][r]);
-          acc[n][r] = fmaf(-mins, dm[r] * (64.f * xs), acc[n][r]);
-        }
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const float main =
+                (c[t][n][0][2 * r] + c[t][n][1][2 * r]) + (c[t][n][0][2 * r + 1] + c[t][n][1][2 * r + 1]);
+            const float mins = cm[t][n][2 * r] + cm[t][n][2 * r + 1];
+            acc[t][n][r] = fmaf(main, dd[t][r] * xs, acc[t][n][r]);
+            acc[t][n][r] = fmaf(-mins, dm[t][r] * (64.f * xs), acc[t][n][r]);
+          }
       }
     }
     __syncwarp();
@@ -451,13 +471,16 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
     ++cstep;
     // ------------------------------------------------ end of a unit
     if (++cw.g == cw.ge) {
-      float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * 32 * NT * 2 + lane * NT * 2;
+      constexpr int PER_LANE = TPW * NT * 2;
+      float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * 32 * PER_LANE + lane * PER_LANE;
 #pragma unroll
-      for (int n = 0; n < NT; ++n) slot[2 * n] = acc[n][0], slot[2 * n + 1] = acc[n][1];
+      for (int t = 0; t < TPW; ++t)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) slot[(t * NT + n) * 2] = acc[t][n][0], slot[(t * NT + n) * 2 + 1] = acc[t][n][1];
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
       if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
         // owner: sum the SLICES partial dot products of every tile and store this chunk's sums
-        const float* rs = red + (size_t)(nunit & 1) * WARPS * 32 * NT * 2 + lane * NT * 2;
+        const float* rs = red + (size_t)(nunit & 1) * WARPS * 32 * PER_LANE + lane * PER_LANE;
         const int row0 = cw.ru * RU;
 #pragma unroll
         for (int cb = 0; cb < COMBOS; ++cb)
@@ -466,9 +489,9 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
             for (int sl = 0; sl < SLICES; ++sl) {
-              const float* q = rs + (size_t)(sl * COMBOS + cb) * 32 * NT * 2;
-              s0 += q[2 * n];
-              s1 += q[2 * n + 1];
+              const float* q = rs + (size_t)(sl * TG + cb / TPW) * 32 * PER_LANE + ((cb % TPW) * NT + n) * 2;
+              s0 += q[0];
+              s1 += q[1];
             }
             const int tok = n * 4 + tig;
             if (tok < P.m) {
@@ -480,7 +503,9 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
           }
       }
 #pragma unroll
-      for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = 0.f;
+      for (int t = 0; t < TPW; ++t)
+#pragma unroll
+        for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = 0.f;
       ++nunit;
       walk_next(cw);
     }
@@ -492,14 +517,16 @@ __global__ void __launch_bounds__(COMBOS * SLICES * 32, 1)
   }
 }
 
-// CTA shapes. Up to 4 tokens: 16 warps (128 registers per thread); K1 loads
-// gate and up boxes of 16 rows x 8 superblocks, K2 one box of 64 rows x 4
-// superblocks. 5-8 tokens: 8 warps, half the superblocks per box, twice the stages.
+// CTA shapes. Up to 4 tokens: 8 warps with two tiles each (gate and up of the
+// same rows; two adjacent W_down tiles) sharing the B fragments they keep in
+// registers; K1 loads gate and up boxes of 16 rows x 8 superblocks, K2 one box
+// of 64 rows x 4 superblocks. 5-8 tokens: 8 warps with one tile each, half the
+// superblocks per box, twice the stages.
 template <bool GATEUP, int NT> struct Shape;
-template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, SLICES = 8, STAGES = 4; };
-template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, SLICES = 4, STAGES = 4; };
-template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, SLICES = 4, STAGES = 8; };
-template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, SLICES = 2, STAGES = 8; };
+template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 4; };
+template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4; };
+template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 8; };
+template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 1, SLICES = 2, STAGES = 8; };
 
 template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
@@ -526,7 +553,7 @@ template <bool GATEUP, int NT>
 cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                         cudaStream_t s) {
   using S = Shape<GATEUP, NT>;
-  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::SLICES, S::STAGES>;
+  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES>;
   constexpr size_t smem = gemv_smem<GATEUP, NT>();
   static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
   int dev = 0;
@@ -538,7 +565,7 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
     if (dev < 64) attr_set |= 1ull << dev;
   }
   void* args[] = {const_cast<CUtensorMap*>(&t0), const_cast<CUtensorMap*>(&t1), const_cast<GemvParams*>(&P)};
-  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS * S::SLICES * 32), smem, s,
+  return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS / S::TPW * S::SLICES * 32), smem, s,
                     args);
 }
 
