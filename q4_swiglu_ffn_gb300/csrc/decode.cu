@@ -216,8 +216,8 @@ __device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* tm, int r
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
 // COMBOS consecutive tiles of W_down); each warp takes TPW of them (sharing the
 // B operand) at one of the SLICES superblocks.
-template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES>
-__global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, 1)
+template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>
+__global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams P) {
   constexpr int TG = COMBOS / TPW;  // tile groups
@@ -517,16 +517,18 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, 1)
   }
 }
 
-// CTA shapes. Up to 4 tokens: 8 warps with two tiles each (gate and up of the
-// same rows; two adjacent W_down tiles) sharing the B fragments they keep in
-// registers; K1 loads gate and up boxes of 16 rows x 8 superblocks, K2 one box
-// of 64 rows x 4 superblocks. 5-8 tokens: 8 warps with one tile each, half the
-// superblocks per box, twice the stages.
+// CTA shapes. Up to 4 tokens: two CTAs per SM (they drift apart, so one's
+// loads and waits overlap the other's arithmetic), each of 8 warps with two
+// tiles per warp (gate and up of the same rows; two adjacent W_down tiles)
+// sharing the B fragments they keep in registers, and a ring of two stages: K1
+// loads gate and up boxes of 16 rows x 8 superblocks, K2 one box of 64 rows x 4
+// superblocks. 5-8 tokens: one CTA per SM of 8 warps with one tile each, half
+// the superblocks per box, eight stages.
 template <bool GATEUP, int NT> struct Shape;
-template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 4; };
-template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4; };
-template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 8; };
-template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 1, SLICES = 2, STAGES = 8; };
+template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
+template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2; };
+template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 8, CPS = 1; };
+template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 1, SLICES = 2, STAGES = 8, CPS = 1; };
 
 template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
@@ -553,7 +555,7 @@ template <bool GATEUP, int NT>
 cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                         cudaStream_t s) {
   using S = Shape<GATEUP, NT>;
-  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES>;
+  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES, S::CPS>;
   constexpr size_t smem = gemv_smem<GATEUP, NT>();
   static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
   int dev = 0;
@@ -624,10 +626,12 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   // at most 16 chunks x 4 tokens of partial sums: with hidden, inter <= 16384 the
   // whole workspace stays under 13.1 MiB
   const int max_nks = 16 / p->nt;
-  choose_split((nsb1 + sl1 - 1) / sl1, nru1, num_sms, max_nks, &p->nks1, &p->kc1);
-  choose_split((nsb2 + sl2 - 1) / sl2, nru2, num_sms, max_nks, &p->nks2, &p->kc2);
-  p->grid1 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks1 * nru1);
-  p->grid2 = (int)std::min<int64_t>(num_sms, (int64_t)p->nks2 * nru2);
+  const int ctas1 = num_sms * (one ? Shape<true, 1>::CPS : Shape<true, 2>::CPS);
+  const int ctas2 = num_sms * (one ? Shape<false, 1>::CPS : Shape<false, 2>::CPS);
+  choose_split((nsb1 + sl1 - 1) / sl1, nru1, ctas1, max_nks, &p->nks1, &p->kc1);
+  choose_split((nsb2 + sl2 - 1) / sl2, nru2, ctas2, max_nks, &p->nks2, &p->kc2);
+  p->grid1 = (int)std::min<int64_t>(ctas1, (int64_t)p->nks1 * nru1);
+  p->grid2 = (int)std::min<int64_t>(ctas2, (int64_t)p->nks2 * nru2);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
