@@ -156,7 +156,8 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
     float g[8], u[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
-    for (int k = 0; k < nks; ++k) {
+#pragma unroll 4
+    for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
       float a[8], b[8];
       load8(part + (((int64_t)k * 2 + 0) * m + t) * inter + i0, a);
       load8(part + (((int64_t)k * 2 + 1) * m + t) * inter + i0, b);
@@ -176,7 +177,8 @@ __global__ void finish_down_kernel(const float* __restrict__ part, int nks, int6
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (4 * i >= n) return;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < nks; ++k) {
+#pragma unroll 8
+  for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
     const float4 a = reinterpret_cast<const float4*>(part + (int64_t)k * n)[i];
     s.x += a.x, s.y += a.y, s.z += a.z, s.w += a.w;
   }
@@ -707,8 +709,9 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
     int64_t n = (int64_t)p.m * p.hidden;
     float* yy = y;
     void* args[] = {&pp, &nks, &n, &yy};
-    e = launch_pdl(reinterpret_cast<const void*>(finish_down_kernel), dim3((unsigned)((n / 4 + 255) / 256)),
-                   dim3(256), 0, s, args);
+    // small CTAs spread the sums over more SMs (more loads in flight)
+    e = launch_pdl(reinterpret_cast<const void*>(finish_down_kernel), dim3((unsigned)((n / 4 + 63) / 64)), dim3(64),
+                   0, s, args);
   }
   prof.after(4, s);
   return e;
