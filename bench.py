@@ -195,21 +195,26 @@ def gpu_decode(args, rank, world, dist):
     gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index if world == 1 else 0]
     sampler = ClockSampler(gpu_index.strip())
     time.sleep(0.5)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # an event after every replay of G steps: the spread of per-step times
+    evr = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    for e in evr:
+        e.record(stream)  # torch creates the CUDA event on first record
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    e0.record(stream)
-    for _ in range(n_rep):
+    evr[0].record(stream)
+    for i in range(n_rep):
         graph.replay()
-    e1.record(stream)
+        evr[i + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist:
         dist.barrier()
     sampler.stop()
-    ms = e0.elapsed_time(e1)
+    ms = evr[0].elapsed_time(evr[-1])
+    per_step = sorted(evr[i].elapsed_time(evr[i + 1]) / G for i in range(n_rep))
+    pct = {q: per_step[min(n_rep - 1, int(q / 100 * n_rep))] for q in (10, 50, 90)}
     clocks = sampler.summary(t0, t1)
 
     # per-kernel durations (events around each kernel of the call; serialises them)
@@ -245,7 +250,7 @@ def gpu_decode(args, rank, world, dist):
     assert q.q4k_check_device_error() == 0
     launches = 4 + (1 if kern_ms[4] > 1e-4 else 0)
     return {"ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "E": E, "R": R,
-            "wbytes": wbytes, "xbytes": x_np.nbytes, "launches_per_step": launches}
+            "wbytes": wbytes, "xbytes": x_np.nbytes, "launches_per_step": launches, "pct": pct, "G": G}
 
 
 def gpu_prefill(args):
@@ -363,7 +368,9 @@ def main():
             "step_frac": (r["wbytes"] / (ms / r["K"] * 1e-3) / 1e9) / pk["hbm_gbs"]}
     e2e_val = r["wbytes"] * r["E"] / (r["e2e_ms"] * 1e-3) / 1e9
     line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": r["K"],
-            "warmup": args.warmup, "ms_per_step": ms / r["K"], "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms / r["K"],
+            "ms_per_step_p10_p50_p90": [r["pct"][10], r["pct"][50], r["pct"][90]],
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f16",
             "data": "synthetic",
             "config": dict(workload, l2=f"rotating {r['R']} weight replicas ({r['R'] * r['wbytes'] / 1e6:.0f} MB "

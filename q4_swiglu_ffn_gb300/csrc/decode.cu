@@ -519,18 +519,17 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes. Up to 4 tokens: two CTAs per SM (they drift apart, so one's
-// loads and waits overlap the other's arithmetic), each of 8 warps with two
-// tiles per warp (gate and up of the same rows; two adjacent W_down tiles)
-// sharing the B fragments they keep in registers, and a ring of two stages: K1
-// loads gate and up boxes of 16 rows x 8 superblocks, K2 one box of 64 rows x 4
-// superblocks. 5-8 tokens: one CTA per SM of 8 warps with one tile each, half
-// the superblocks per box, eight stages.
+// CTA shapes: 8 warps with two tiles per warp (gate and up of the same rows;
+// two adjacent W_down tiles) sharing the B operand. K1 loads gate and up boxes
+// of 16 rows x 8 superblocks, K2 one box of 64 rows x 4 superblocks (36.9 KB
+// per stage). Up to 4 tokens: two CTAs per SM (they drift apart, so one's loads
+// and waits overlap the other's arithmetic), two stages each, B kept in
+// registers. 5-8 tokens (two token tiles): one CTA per SM, four stages.
 template <bool GATEUP, int NT> struct Shape;
 template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
 template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2; };
-template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 8, CPS = 1; };
-template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 1, SLICES = 2, STAGES = 8, CPS = 1; };
+template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 4, CPS = 1; };
+template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4, CPS = 1; };
 
 template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
