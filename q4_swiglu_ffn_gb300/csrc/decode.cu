@@ -576,15 +576,10 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
 // block, rows, blocks}; a box of box_rows rows x slices superblocks lands in
 // shared memory superblock-major, 144 bytes per row.
 bool weight_map(CUtensorMap* m, const void* w, int rows, int nsb, int box_rows, int slices) {
-  auto fn = tmap_encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)(BLK / 8), (cuuint64_t)rows, (cuuint64_t)nsb};
-  cuuint64_t strides[2] = {(cuuint64_t)nsb * BLK, (cuuint64_t)BLK};
-  cuuint32_t box[3] = {(cuuint32_t)(BLK / 8), (cuuint32_t)box_rows, (cuuint32_t)slices};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, const_cast<void*>(w), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[3] = {(cuuint64_t)(BLK / 8), (cuuint64_t)rows, (cuuint64_t)nsb};
+  const cuuint64_t strides[2] = {(cuuint64_t)nsb * BLK, (cuuint64_t)BLK};
+  const cuuint32_t box[3] = {(cuuint32_t)(BLK / 8), (cuuint32_t)box_rows, (cuuint32_t)slices};
+  return tmap_encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Number of K-chunks: the most, up to max_nks, among those that minimise the longest CTA's
