@@ -156,10 +156,20 @@ q4k_status q4k_dequantize(const void* q4k, int64_t rows, int64_t cols, float* ou
  * Q4K_ERR_CUDA (a sticky runtime error). */
 q4k_status q4k_check_device_error(q4k_stream_t stream);
 
+/* Test hook for the bounded device waits (no counterpart on the source pages).
+ * Enqueues on `stream` one warp that waits, through the same bounded wait as
+ * the FFN kernels, on a barrier that nothing completes. The wait gives up after
+ * limit_ns nanoseconds (1e3..2e9; otherwise Q4K_ERR_SHAPE, nothing launched)
+ * and records a timeout in the device error word, so that the next
+ * q4k_check_device_error() returns Q4K_ERR_TIMEOUT and the context stays
+ * usable. No memory of the caller is touched. */
+q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream);
+
 /* Per-kernel timing hook (for benchmarks). After this call, every FFN call made
  * on this thread records events[2i] (cudaEvent_t) before and events[2i+1] after
- * its i-th kernel, for i < n/2, on the call's stream. Decode calls launch 3
- * kernels (activation fragments, gate+up+SwiGLU, down), prefill calls 5 (Q8_1
+ * its i-th kernel, for i < n/2, on the call's stream. Decode calls launch up to
+ * 5 (activation fragments, gate+up GEMV, chunk sum + SwiGLU + h fragments, down
+ * GEMV, down chunk sum when K is split), prefill calls 5 (Q8_1
  * of x, operand expansion, gate+up MMQ + SwiGLU + Q8_1 of h, operand expansion,
  * down MMQ). The events stay owned by the caller; n = 0 (events NULL) turns the
  * hook off. Recording between kernels serialises them, so timed runs of the

@@ -36,6 +36,7 @@ _SIGS = {
     "ffn_q4k_workspace_h_q8_1_offset": (_sz, [_i64, _i64, _i64]),
     "q4k_dequantize": (_int, [_p, _i64, _i64, _p, _p]),
     "q4k_check_device_error": (_int, [_p]),
+    "q4k_test_bounded_wait": (_int, [ctypes.c_uint64, _p]),
     "q4k_set_profile_events": (_int, [_p, _int]),
     "q4k_get_last_error": (_int, []),
     "q4k_status_string": (ctypes.c_char_p, [_int]),
@@ -151,6 +152,11 @@ def q4k_dequantize(q, rows: int, cols: int, out=None, stream=None):
 def q4k_check_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error status code."""
     return lib.q4k_check_device_error(_stream(stream))
+
+
+def q4k_test_bounded_wait(limit_ns: int, stream=None) -> None:
+    """Enqueue a wait that nothing completes; it gives up after limit_ns and records a timeout."""
+    _check(lib.q4k_test_bounded_wait(int(limit_ns), _stream(stream)), "q4k_test_bounded_wait")
 
 
 def q4k_set_profile_events(events) -> None:

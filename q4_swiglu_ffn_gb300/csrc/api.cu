@@ -223,6 +223,30 @@ q4k_status q4k_check_device_error(q4k_stream_t stream) {
   return Q4K_OK;
 }
 
+namespace {
+// One warp waits on an mbarrier that nothing will complete, through the same
+// bounded wait as the FFN kernels, then returns: the wait gives up after
+// limit_ns and records the timeout in the device error word.
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    q4k::mbar_init(&bar, 1);
+    q4k::fence_mbar_init();
+  }
+  __syncwarp();
+  (void)q4k::mbar_wait(&bar, 0u, err, limit_ns);
+}
+}  // namespace
+
+q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > q4k::WAIT_LIMIT_NS) return fail(Q4K_ERR_SHAPE);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  bounded_wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(limit_ns, d->err);
+  return cudaGetLastError() == cudaSuccess ? Q4K_OK : fail(Q4K_ERR_CUDA);
+}
+
 q4k_status q4k_set_profile_events(void* const* events, int n) {
   if (n < 0 || (n > 0 && !events)) return fail(Q4K_ERR_NULL);
   g_prof.ev = n > 0 ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events)) : nullptr;
