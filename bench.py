@@ -299,6 +299,20 @@ def gpu_prefill(args):
     return {"ms": ms, "kern_ms": kern_ms, "ops": cfg.int8_ops(), "cfg": cfg}
 
 
+def whole_job(ms_local: float, units_local: float, dist=None):
+    """Max over ranks of the timed region (ms) and the whole-job rate: units summed
+    over all ranks (each rank does the same work) divided by that time."""
+    ms, world = ms_local, 1
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, units_local * world / (ms * 1e-3)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -338,13 +352,8 @@ def main():
         __graft_entry__.build()
 
     r = gpu_decode(args, rank, world, dist)
-    ms = r["ms"]
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    units = r["wbytes"] * r["K"] * world
-    value = units / (ms * 1e-3) / 1e9
+    ms, rate = whole_job(r["ms"], r["wbytes"] * r["K"], dist)
+    value = rate / 1e9
     pk, pk_kind = peaks()
 
     pre = None
