@@ -335,10 +335,10 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   // With up to 4 tokens a warp keeps the B fragments of its superblock in
   // registers for as long as that superblock stays the same (with one group per
   // K-chunk: until its chunk changes).
-  constexpr bool CACHE_B = NT == 1;
-  uint2 bc[CACHE_B ? 16 : 1];
-  uint32_t bmc = 0;
-  float xsc = 0.f;
+  constexpr bool CACHE_B = true;
+  uint2 bc[16][NT];
+  uint32_t bmc[NT];
+  float xsc[NT];
   int csb = -1;
 
   // A warp whose wait timed out raises the CTA's abort flag and stops waiting,
@@ -406,9 +406,14 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
       if (CACHE_B && sb != csb) {
 #pragma unroll
-        for (int k = 0; k < (CACHE_B ? 16 : 1); ++k) bc[k] = fx[k * 32 + flane[0]];
-        bmc = P.in.fm[(int64_t)sb * 32 + flane[0]];
-        xsc = P.in.sc[(int64_t)sb * 8 + tig];
+        for (int k = 0; k < 16; ++k)
+#pragma unroll
+          for (int n = 0; n < NT; ++n) bc[k][n] = fx[(k * NT + n) * 32 + flane[n]];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          bmc[n] = P.in.fm[((int64_t)sb * NT + n) * 32 + flane[n]];
+          xsc[n] = P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
+        }
         csb = sb;
       }
 #pragma unroll
@@ -417,8 +422,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           if (CACHE_B) {
-            b0[n] = bc[(2 * w) % (CACHE_B ? 16 : 1)];
-            b1[n] = bc[(2 * w + 1) % (CACHE_B ? 16 : 1)];
+            b0[n] = bc[2 * w][n];
+            b1[n] = bc[2 * w + 1][n];
           } else {
             b0[n] = fx[((2 * w) * NT + n) * 32 + flane[n]];
             b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
@@ -448,14 +453,14 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         const uint32_t* fm = P.in.fm + (int64_t)sb * NT * 32;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const uint32_t bm = CACHE_B ? bmc : fm[n * 32 + flane[n]];
+          const uint32_t bm = CACHE_B ? bmc[n] : fm[n * 32 + flane[n]];
 #pragma unroll
           for (int t = 0; t < TPW; ++t) mma16816(cm[t][n], A_min[t][0], A_min[t][1], 0u, 0u, bm, 0u);
         }
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float xs = CACHE_B ? xsc : P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
+        const float xs = CACHE_B ? xsc[n] : P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
 #pragma unroll
         for (int t = 0; t < TPW; ++t)
 #pragma unroll
