@@ -87,13 +87,91 @@ size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
   return q4k::prefill_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
 }
 
+// Decode calls repeat with the same buffers token after token, so each distinct
+// call (buffers, shape, dtype) is recorded once as a CUDA graph of its kernel
+// launches and replayed afterwards: one graph launch instead of five kernel
+// launches. The first call of a kind runs directly (which also prepares each
+// kernel) and then records the graph on a private stream. Calls made while the
+// caller's stream is being captured, or with the profiling hook on, launch
+// directly.
+struct DecodeGraph {
+  bool used = false;
+  const void *x = nullptr, *wg = nullptr, *wu = nullptr, *wd = nullptr, *ws = nullptr;
+  float* y = nullptr;
+  int dtype = 0;
+  int64_t m = 0, hidden = 0, inter = 0;
+  uint64_t last = 0;
+  cudaGraphExec_t exec = nullptr;
+};
+struct GraphCache {
+  static constexpr int N = 32;
+  std::mutex mu;
+  DecodeGraph g[N];
+  uint64_t tick = 0;
+  cudaStream_t cap = nullptr;  // private stream the graphs are recorded on
+};
+GraphCache g_graphs[MAX_DEV];
+
+q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
+                      const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+  int dev = 0;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  const bool graphs = !g_prof.ev && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < MAX_DEV &&
+                      cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone;
+  if (!graphs) {
+    return q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof) == cudaSuccess
+               ? Q4K_OK
+               : Q4K_ERR_CUDA;
+  }
+  GraphCache& gc = g_graphs[dev];
+  std::lock_guard<std::mutex> lk(gc.mu);
+  ++gc.tick;
+  for (DecodeGraph& g : gc.g)
+    if (g.used && g.x == x && g.y == y && g.wg == wg && g.wu == wu && g.wd == wd && g.ws == ws && g.dtype == dtype &&
+        g.m == p.m && g.hidden == p.hidden && g.inter == p.inter) {
+      g.last = gc.tick;
+      return cudaGraphLaunch(g.exec, s) == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+    }
+  // first call of this kind: run it directly, then record it for the next ones
+  if (q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, q4k::ProfileEvents{}) !=
+      cudaSuccess)
+    return Q4K_ERR_CUDA;
+  if (!gc.cap && cudaStreamCreateWithFlags(&gc.cap, cudaStreamNonBlocking) != cudaSuccess) {
+    gc.cap = nullptr;
+    return Q4K_OK;  // no graph this time; the call itself has been issued
+  }
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamBeginCapture(gc.cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return Q4K_OK;
+  const cudaError_t le = q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, gc.cap,
+                                            q4k::ProfileEvents{});
+  const cudaError_t ce = cudaStreamEndCapture(gc.cap, &graph);
+  cudaGraphExec_t exec = nullptr;
+  if (le != cudaSuccess || ce != cudaSuccess || !graph || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    (void)cudaGetLastError();  // a failed recording leaves the direct path as it was
+    return Q4K_OK;
+  }
+  cudaGraphDestroy(graph);
+  DecodeGraph* slot = &gc.g[0];
+  for (DecodeGraph& g : gc.g) {
+    if (!g.used) {
+      slot = &g;
+      break;
+    }
+    if (g.last < slot->last) slot = &g;
+  }
+  if (slot->used) cudaGraphExecDestroy(slot->exec);  // freed once any launch in flight completes
+  *slot = DecodeGraph{true, x, wg, wu, wd, ws, y, dtype, p.m, p.hidden, p.inter, gc.tick, exec};
+  return Q4K_OK;
+}
+
 q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t inter, const void* wg,
                    const void* wu, const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
   cudaError_t e;
   if (is_decode(m)) {
     q4k::DecodePlan p;
     if (!q4k::decode_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
-    e = q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof);
+    return run_decode(p, x, dtype, wg, wu, wd, y, ws, d, s);
   } else {
     q4k::PrefillPlan p;
     if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;

@@ -56,6 +56,31 @@ def test_decode_repeatable_and_deterministic():
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
 
 
+def test_decode_repeated_calls_on_the_same_buffers():
+    """A decode loop calls with the same buffers every token; such repeats are replayed
+    from a recorded launch sequence, which must read the current x every time."""
+    c = workloads.small_config(1024, 2816, 2)
+    wg, wu, wd = workloads.weights(c)
+    dg, du, dd = to_dev(wg), to_dev(wu), to_dev(wd)
+    xd = torch.empty((2, 1024), dtype=torch.float32, device=dev())
+    y = torch.empty((2, 1024), dtype=torch.float32, device=dev())
+    outs = []
+    for k in range(4):
+        x, _ = workloads.activations(c, seed=c.seed + 17 * k)
+        xd.copy_(torch.from_numpy(x))
+        lib().ffn_q4k_swiglu(xd, dg, du, dd, y=y)
+        torch.cuda.synchronize()
+        ref, _ = oracle.ffn_decode(x, wg, wu, wd)
+        assert rel_l2(y.cpu().numpy(), ref) <= DECODE_TIGHT, k
+        outs.append(y.cpu().numpy().copy())
+    x, _ = workloads.activations(c, seed=c.seed)  # the first input again: the same bits
+    xd.copy_(torch.from_numpy(x))
+    lib().ffn_q4k_swiglu(xd, dg, du, dd, y=y)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), outs[0].view(np.uint32))
+    assert lib().q4k_check_device_error() == 0
+
+
 def test_decode_special_inputs():
     c = workloads.small_config(512, 768, 3)
     wg, wu, wd = workloads.weights(c)
