@@ -1,5 +1,6 @@
 // C ABI of the Q4_K SwiGLU FFN library: argument validation, per-device state
-// (architecture check, error word, default workspace) and dispatch by regime.
+// (architecture check, error word, default workspace), dispatch by regime, and
+// replay of repeated decode calls from recorded CUDA graphs.
 // Conventions (see include/q4kffn.h): device pointers owned by the caller,
 // work enqueued on the caller's stream without synchronisation, argument
 // errors returned before anything is launched (realizar

@@ -30,13 +30,14 @@
 // 16-row tiles (gate and up of one tile in K1, four consecutive tiles of
 // W_down in K2) over one K-chunk. Each step loads, with one 3-D TMA box per
 // matrix, the next group of SLICES consecutive superblocks of those rows
-// (1152 or 576 contiguous bytes per row, which DRAM streams efficiently) into
-// a stage of a ring shared by the CTA; in shared memory the box is laid out
+// (1152 or 576 contiguous bytes per row) into a stage of a ring shared by the
+// CTA; in shared memory the box is laid out
 // superblock-major, 144 bytes per row, so the fragment loads are free of bank
-// conflicts. Warp w processes tile (w % COMBOS) at superblock (w / COMBOS) of
-// the group. At the end of a unit an owner warp (rotating) sums the SLICES
-// partial dot products through shared memory and stores them; the chunks are
-// summed by K1b / K3 in a fixed order, so results are deterministic.
+// conflicts. Each warp takes TPW of the unit's tiles at one superblock of the
+// group and keeps that superblock's B fragments in registers while it stays the
+// same. At the end of a unit an owner warp (rotating) sums the SLICES partial
+// dot products through shared memory and stores them; the chunks are summed by
+// K1b / K3 in a fixed order, so results are deterministic.
 #include <algorithm>
 #include <cmath>
 
@@ -332,10 +333,9 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   for (int t = 0; t < TPW; ++t)
 #pragma unroll
     for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = 0.f;
-  // With up to 4 tokens a warp keeps the B fragments of its superblock in
-  // registers for as long as that superblock stays the same (with one group per
-  // K-chunk: until its chunk changes).
-  constexpr bool CACHE_B = true;
+  // A warp keeps the B fragments of its superblock in registers for as long as
+  // that superblock stays the same (with one group per K-chunk: until its chunk
+  // changes).
   uint2 bc[16][NT];
   uint32_t bmc[NT];
   float xsc[NT];
@@ -403,8 +403,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int i = 0; i < 4; ++i) c[t][n][0][i] = c[t][n][1][i] = cm[t][n][i] = 0.f;
-      const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
-      if (CACHE_B && sb != csb) {
+      if (sb != csb) {
+        const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
 #pragma unroll
         for (int k = 0; k < 16; ++k)
 #pragma unroll
@@ -421,13 +421,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         uint2 b0[NT], b1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          if (CACHE_B) {
-            b0[n] = bc[2 * w][n];
-            b1[n] = bc[2 * w + 1][n];
-          } else {
-            b0[n] = fx[((2 * w) * NT + n) * 32 + flane[n]];
-            b1[n] = fx[((2 * w + 1) * NT + n) * 32 + flane[n]];
-          }
+          b0[n] = bc[2 * w][n];
+          b1[n] = bc[2 * w + 1][n];
         }
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
@@ -450,17 +445,16 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         }
       }
       {
-        const uint32_t* fm = P.in.fm + (int64_t)sb * NT * 32;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          const uint32_t bm = CACHE_B ? bmc[n] : fm[n * 32 + flane[n]];
+          const uint32_t bm = bmc[n];
 #pragma unroll
           for (int t = 0; t < TPW; ++t) mma16816(cm[t][n], A_min[t][0], A_min[t][1], 0u, 0u, bm, 0u);
         }
       }
 #pragma unroll
       for (int n = 0; n < NT; ++n) {
-        const float xs = CACHE_B ? xsc[n] : P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
+        const float xs = xsc[n];
 #pragma unroll
         for (int t = 0; t < TPW; ++t)
 #pragma unroll
@@ -528,8 +522,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 // two adjacent W_down tiles) sharing the B operand. K1 loads gate and up boxes
 // of 16 rows x 8 superblocks, K2 one box of 64 rows x 4 superblocks (36.9 KB
 // per stage). Up to 4 tokens: two CTAs per SM (they drift apart, so one's loads
-// and waits overlap the other's arithmetic), two stages each, B kept in
-// registers. 5-8 tokens (two token tiles): one CTA per SM, four stages.
+// and waits overlap the other's arithmetic), two stages each. 5-8 tokens (two
+// token tiles, twice the registers for B): one CTA per SM, four stages.
 template <bool GATEUP, int NT> struct Shape;
 template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
 template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2; };
