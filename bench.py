@@ -62,9 +62,21 @@ def peaks():
 
 
 def src_hash(*files) -> str:
+    """Hash of the code that decides the profiled kernel's memory traffic: the GEMV
+    kernel template and its CTA shapes in decode.cu, plus the named helper files,
+    with comments and blank space removed (edits to comments or to other kernels
+    keep a committed profile valid)."""
+    import re
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, "q4_swiglu_ffn_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "q4_swiglu_ffn_gb300", "csrc", f)).read()
+        if f == "decode.cu":
+            a = text.index("template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>")
+            b = text.index("constexpr size_t gemv_smem()")
+            text = text[a:b]
+        text = re.sub(r"//[^\n]*", "", text)
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        h.update(re.sub(r"\s+", "", text).encode())
     return h.hexdigest()[:16]
 
 
