@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill-steps", type=int, default=120)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-q8", action="store_true", help="skip the Q8_1-activation decode leg")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -169,7 +170,9 @@ def cpu_baseline(budget_s: float):
 
 
 # --------------------------------------------------------------------------- GPU side
-def gpu_decode(args, rank, world, dist):
+def gpu_decode(args, rank, world, dist, path="f32"):
+    """Times the decode FFN call: `path` "f32" is ffn_q4k_swiglu (float32 activations),
+    "q8_1" is ffn_q4k_swiglu_q8_1 (activations quantized to Q8_1, integer dot products)."""
     import numpy as np
     import torch
     import workloads
@@ -187,9 +190,17 @@ def gpu_decode(args, rank, world, dist):
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
 
-    def step(i):
-        wg, wu, wd = reps[i % R]
-        q.ffn_q4k_swiglu(x, wg, wu, wd, y=y)
+    if path == "q8_1":
+        ws = torch.empty(q.ffn_q4k_q8_1_workspace_bytes(cfg.m, cfg.hidden, cfg.inter), dtype=torch.uint8,
+                         device=dev)
+
+        def step(i):
+            wg, wu, wd = reps[i % R]
+            q.ffn_q4k_swiglu_q8_1(x, wg, wu, wd, ws, y=y)
+    else:
+        def step(i):
+            wg, wu, wd = reps[i % R]
+            q.ffn_q4k_swiglu(x, wg, wu, wd, y=y)
 
     for i in range(max(3, args.warmup)):
         step(i)
@@ -247,7 +258,7 @@ def gpu_decode(args, rank, world, dist):
     # end to end: pinned host x in, host y out, every step
     xh = torch.from_numpy(x_np).pin_memory()
     yh = torch.empty(x_np.shape, dtype=torch.float32).pin_memory()
-    E = min(K, 2000)
+    E = min(K, 2000) if path == "f32" else 0
     torch.cuda.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
@@ -375,6 +386,10 @@ def main():
     value = rate / 1e9
     pk, pk_kind = peaks()
 
+    r8 = None
+    if not args.no_q8 and rank == 0:
+        r8 = gpu_decode(args, rank, 1, None, path="q8_1")
+
     pre = None
     if not args.no_prefill and rank == 0:
         pre = gpu_prefill(args)
@@ -412,6 +427,25 @@ def main():
                     "note": "pinned host x -> device, the C-ABI call, device y -> pinned host, stream sync, every step"},
             "gpu_launches": r["launches_per_step"] * r["K"] * world,
             "clocks": r["clocks"]}
+    if r8 is not None:
+        k1q_ms = r8["kern_ms"][1]
+        ach8 = k1_bytes / (k1q_ms * 1e-3) / 1e9
+        line["decode_q8_1"] = {
+            "workload": cfg.name, "value": r8["wbytes"] * r8["K"] / (r8["ms"] * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": r8["ms"] / r8["K"],
+            "ms_per_step_p10_p50_p90": [r8["pct"][10], r8["pct"][50], r8["pct"][90]],
+            "step_frac": (r8["wbytes"] / (r8["ms"] / r8["K"] * 1e-3) / 1e9) / pk["hbm_gbs"],
+            "dtype": "int8 x u4 (dp4a), f32 scales",
+            "numerics": "activations quantized to Q8_1 (x once for gate and up, h before down): "
+                        "not the float32-activation contract of the headline value",
+            "kernels_ms": dict(zip(["q8_1_x", "gate_up", "swiglu_q8_1_h", "down", "down_chunk_sum"],
+                                   r8["kern_ms"])),
+            "roofline": {"kernel": "gemv_q8_kernel<gate/up> (K1)", "bound": "hbm", "achieved": ach8,
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach8 / pk["hbm_gbs"],
+                         "peak_kind": f"{pk_kind} copy bandwidth", "algorithmic_bytes_per_launch": k1_bytes,
+                         "avg_launch_ms": k1q_ms},
+            "gpu_launches": r8["launches_per_step"] * r8["K"],
+            "clocks": r8["clocks"]}
     if pre is not None:
         c = pre["cfg"]
         gu_ops = 2 * c.m * c.hidden * c.inter * 2

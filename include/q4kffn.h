@@ -33,6 +33,7 @@
  *   - Regimes: m <= 8 runs the decode path (float32 activations, no
  *     activation quantization); m >= 9 runs the prefill path (activations
  *     quantized to Q8_1, Q4_K x Q8_1 GEMM on the tensor cores).
+ *     ffn_q4k_swiglu_q8_1 quantizes the activations to Q8_1 at every m.
  */
 #ifndef Q4KFFN_H
 #define Q4KFFN_H
@@ -116,6 +117,33 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
                              const void* W_down, float* y, void* workspace, size_t ws_bytes,
                              q4k_stream_t stream);
 
+/* The feed-forward block with Q8_1 activations at every m: x is quantized to
+ * Q8_1 once and shared by the gate and up projections, h = silu(g) * u is
+ * re-quantized to Q8_1 before the down projection, and every dot product is
+ * the Q4_K x Q8_1 block product
+ *     d * sum_j scale_j * d8_j * sum_i(q_i * q8_i) - dmin * sum_j min_j * s8_j
+ * with exact integer inner sums. Source: realizar src/cuda/executor/layers/
+ * ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (the decode pipeline with quantized
+ * activations and integer dot products); spark_model/layers/ops/q4k_mmq.rs,
+ * q4k_mmq_gemm (the block correction). For m = 1..8 it runs integer-dot GEMVs
+ * (x Q8_1, gate+up GEMV, chunk sum + SwiGLU + Q8_1 of h, down GEMV, down chunk
+ * sum); for m >= 9 it is the same computation as ffn_q4k_swiglu_ex's prefill
+ * path (and gives the same bytes). x is float32 or bf16 [m][hidden] (bf16 is
+ * widened exactly before quantization), y float32 [m][hidden]. The workspace is
+ * caller-owned, 256-byte aligned, of at least ffn_q4k_q8_1_workspace_bytes(m,
+ * hidden, inter) bytes, needs no initialisation, and must not be shared by
+ * calls that overlap on the GPU. Repeated decode calls with the same buffers
+ * are replayed from a recorded CUDA graph, as for ffn_q4k_swiglu. */
+q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden,
+                               int64_t inter, const void* W_gate, const void* W_up,
+                               const void* W_down, float* y, void* workspace, size_t ws_bytes,
+                               q4k_stream_t stream);
+/* Workspace bytes ffn_q4k_swiglu_q8_1 needs for this shape (0 for an invalid shape). */
+size_t ffn_q4k_q8_1_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
+/* Test hook: byte offset, inside an ffn_q4k_swiglu_q8_1 workspace, of the
+ * planar Q8_1 copy of h = silu(gate)*up (q8_1_bytes(m, inter) bytes) that the
+ * call feeds to the down projection; 0 for an invalid shape. */
+size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter);
 /* Decode-regime variant of ffn_q4k_swiglu (float32 x, m = 1..8, hidden and
  * inter multiples of 256 up to 16384) that allocates no device memory, for
  * callers that cannot call cudaMalloc: a serving process whose memory pool owns

@@ -32,6 +32,9 @@ _SIGS = {
     "q8_1_quantize_act": (_int, [_p, _int, _i64, _i64, _p, _p]),
     "ffn_q4k_swiglu": (_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
     "ffn_q4k_swiglu_ex": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
+    "ffn_q4k_swiglu_q8_1": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
+    "ffn_q4k_q8_1_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "ffn_q4k_q8_1_workspace_h_offset": (_sz, [_i64, _i64, _i64]),
     "ffn_q4k_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "ffn_q4k_workspace_h_q8_1_offset": (_sz, [_i64, _i64, _i64]),
     "q4k_dequantize": (_int, [_p, _i64, _i64, _p, _p]),
@@ -90,6 +93,14 @@ def ffn_q4k_workspace_bytes(m: int, hidden: int, inter: int) -> int:
     return lib.ffn_q4k_workspace_bytes(m, hidden, inter)
 
 
+def ffn_q4k_q8_1_workspace_bytes(m: int, hidden: int, inter: int) -> int:
+    return lib.ffn_q4k_q8_1_workspace_bytes(m, hidden, inter)
+
+
+def ffn_q4k_q8_1_workspace_h_offset(m: int, hidden: int, inter: int) -> int:
+    return lib.ffn_q4k_q8_1_workspace_h_offset(m, hidden, inter)
+
+
 def ffn_q4k_workspace_h_q8_1_offset(m: int, hidden: int, inter: int) -> int:
     return lib.ffn_q4k_workspace_h_q8_1_offset(m, hidden, inter)
 
@@ -137,6 +148,19 @@ def ffn_q4k_swiglu_ex(x, W_gate, W_up, W_down, workspace, y=None, stream=None):
     _check(lib.ffn_q4k_swiglu_ex(_ptr(x), _dtype_code(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up),
                                  _ptr(W_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
            "ffn_q4k_swiglu_ex")
+    return y
+
+
+def ffn_q4k_swiglu_q8_1(x, W_gate, W_up, W_down, workspace, y=None, stream=None):
+    """The FFN with Q8_1 activations at every m (x float32 or bf16; caller workspace, uint8 CUDA tensor)."""
+    import torch
+    m, hidden = x.shape
+    inter = W_gate.shape[0]
+    if y is None:
+        y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
+    _check(lib.ffn_q4k_swiglu_q8_1(_ptr(x), _dtype_code(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up),
+                                   _ptr(W_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "ffn_q4k_swiglu_q8_1")
     return y
 
 

@@ -88,15 +88,24 @@ size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
   return q4k::prefill_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
 }
 
+size_t plan_bytes_q8(int64_t m, int64_t hidden, int64_t inter, int sms) {
+  if (is_decode(m)) {
+    q4k::DecodeQ8Plan p;
+    return q4k::decode_q8_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
+  }
+  return plan_bytes(m, hidden, inter, sms);
+}
+
 // Decode calls repeat with the same buffers token after token, so each distinct
-// call (buffers, shape, dtype) is recorded once as a CUDA graph of its kernel
-// launches and replayed afterwards: one graph launch instead of five kernel
-// launches. The first call of a kind runs directly (which also prepares each
-// kernel) and then records the graph on a private stream. Calls made while the
-// caller's stream is being captured, or with the profiling hook on, launch
+// call (path, buffers, shape, dtype) is recorded once as a CUDA graph of its
+// kernel launches and replayed afterwards: one graph launch instead of five
+// kernel launches. The first call of a kind runs directly (which also prepares
+// each kernel) and then records the graph on a private stream. Calls made while
+// the caller's stream is being captured, or with the profiling hook on, launch
 // directly.
 struct DecodeGraph {
   bool used = false;
+  int path = 0;  // 0: float32 activations, 1: Q8_1 activations
   const void *x = nullptr, *wg = nullptr, *wu = nullptr, *wd = nullptr, *ws = nullptr;
   float* y = nullptr;
   int dtype = 0;
@@ -113,38 +122,33 @@ struct GraphCache {
 };
 GraphCache g_graphs[MAX_DEV];
 
-q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
-                      const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+// `launch(stream, profile)` enqueues the call's kernels on `stream`.
+template <class Launch>
+q4k_status run_graphed(const DecodeGraph& key, cudaStream_t s, Launch launch) {
   int dev = 0;
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   const bool graphs = !g_prof.ev && cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < MAX_DEV &&
                       cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone;
-  if (!graphs) {
-    return q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof) == cudaSuccess
-               ? Q4K_OK
-               : Q4K_ERR_CUDA;
-  }
+  if (!graphs) return launch(s, g_prof) == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
   GraphCache& gc = g_graphs[dev];
   std::lock_guard<std::mutex> lk(gc.mu);
   ++gc.tick;
   for (DecodeGraph& g : gc.g)
-    if (g.used && g.x == x && g.y == y && g.wg == wg && g.wu == wu && g.wd == wd && g.ws == ws && g.dtype == dtype &&
-        g.m == p.m && g.hidden == p.hidden && g.inter == p.inter) {
+    if (g.used && g.path == key.path && g.x == key.x && g.y == key.y && g.wg == key.wg && g.wu == key.wu &&
+        g.wd == key.wd && g.ws == key.ws && g.dtype == key.dtype && g.m == key.m && g.hidden == key.hidden &&
+        g.inter == key.inter) {
       g.last = gc.tick;
       return cudaGraphLaunch(g.exec, s) == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
     }
   // first call of this kind: run it directly, then record it for the next ones
-  if (q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, q4k::ProfileEvents{}) !=
-      cudaSuccess)
-    return Q4K_ERR_CUDA;
+  if (launch(s, q4k::ProfileEvents{}) != cudaSuccess) return Q4K_ERR_CUDA;
   if (!gc.cap && cudaStreamCreateWithFlags(&gc.cap, cudaStreamNonBlocking) != cudaSuccess) {
     gc.cap = nullptr;
     return Q4K_OK;  // no graph this time; the call itself has been issued
   }
   cudaGraph_t graph = nullptr;
   if (cudaStreamBeginCapture(gc.cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return Q4K_OK;
-  const cudaError_t le = q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, gc.cap,
-                                            q4k::ProfileEvents{});
+  const cudaError_t le = launch(gc.cap, q4k::ProfileEvents{});
   const cudaError_t ce = cudaStreamEndCapture(gc.cap, &graph);
   cudaGraphExec_t exec = nullptr;
   if (le != cudaSuccess || ce != cudaSuccess || !graph || cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
@@ -162,8 +166,33 @@ q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const 
     if (g.last < slot->last) slot = &g;
   }
   if (slot->used) cudaGraphExecDestroy(slot->exec);  // freed once any launch in flight completes
-  *slot = DecodeGraph{true, x, wg, wu, wd, ws, y, dtype, p.m, p.hidden, p.inter, gc.tick, exec};
+  *slot = key;
+  slot->used = true;
+  slot->last = gc.tick;
+  slot->exec = exec;
   return Q4K_OK;
+}
+
+q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
+                      const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+  DecodeGraph key;
+  key.path = 0;
+  key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = y;
+  key.dtype = dtype, key.m = p.m, key.hidden = p.hidden, key.inter = p.inter;
+  return run_graphed(key, s, [&](cudaStream_t st, const q4k::ProfileEvents& pr) {
+    return q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, st, pr);
+  });
+}
+
+q4k_status run_decode_q8(const q4k::DecodeQ8Plan& p, const void* x, int dtype, const void* wg, const void* wu,
+                         const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+  DecodeGraph key;
+  key.path = 1;
+  key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = y;
+  key.dtype = dtype, key.m = p.m, key.hidden = p.hidden, key.inter = p.inter;
+  return run_graphed(key, s, [&](cudaStream_t st, const q4k::ProfileEvents& pr) {
+    return q4k::launch_decode_q8(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, st, pr);
+  });
 }
 
 q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t inter, const void* wg,
@@ -261,6 +290,48 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
   if (ws_bytes < need) return fail(Q4K_ERR_NOMEM);
   st = run_ffn(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
   return st == Q4K_OK ? st : fail(st);
+}
+
+q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden, int64_t inter,
+                               const void* W_gate, const void* W_up, const void* W_down, float* y, void* workspace,
+                               size_t ws_bytes, q4k_stream_t stream) {
+  q4k_status st = check_ffn_args(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y);
+  if (st != Q4K_OK) return fail(st);
+  if (!workspace) return fail(Q4K_ERR_NULL);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  const size_t need = plan_bytes_q8(m, hidden, inter, d->sms);
+  if (need == 0) return fail(Q4K_ERR_SHAPE);
+  if (ws_bytes < need) return fail(Q4K_ERR_NOMEM);
+  if (!is_decode(m)) {  // the prefill path already quantizes its activations to Q8_1
+    st = run_ffn(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
+    return st == Q4K_OK ? st : fail(st);
+  }
+  q4k::DecodeQ8Plan p;
+  if (!q4k::decode_q8_plan(m, hidden, inter, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
+  st = run_decode_q8(p, x, dtype, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
+  return st == Q4K_OK ? st : fail(st);
+}
+
+size_t ffn_q4k_q8_1_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {
+  if (!tokens_ok(m) || !dim_ok(hidden) || !dim_ok(inter)) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != Q4K_OK) return 0;
+  return plan_bytes_q8(m, hidden, inter, d->sms);
+}
+
+size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter) {
+  if (!tokens_ok(m) || !dim_ok(hidden) || !dim_ok(inter)) return 0;
+  DeviceState* d = nullptr;
+  if (device_state(&d) != Q4K_OK) return 0;
+  if (is_decode(m)) {
+    q4k::DecodeQ8Plan p;
+    return q4k::decode_q8_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
+  }
+  q4k::PrefillPlan p;
+  return q4k::prefill_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
 }
 
 size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {

@@ -42,8 +42,8 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "gemv_stream.cuh"
 #include "kernels.h"
-#include "tmap.h"
 
 namespace q4k {
 
@@ -171,21 +171,6 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
   frag_token(v, t >= m, t, nt, sb, f);
 }
 
-// K3: y = sum over the K-chunks of the down partials, in chunk order.
-__global__ void finish_down_kernel(const float* __restrict__ part, int nks, int64_t n, float* __restrict__ y) {
-  pdl_launch_dependents();
-  pdl_wait();
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (4 * i >= n) return;
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
-    const float4 a = reinterpret_cast<const float4*>(part + (int64_t)k * n)[i];
-    s.x += a.x, s.y += a.y, s.z += a.z, s.w += a.w;
-  }
-  reinterpret_cast<float4*>(y)[i] = s;
-}
-
 struct GemvParams {
   int rows;           // output rows of each matrix
   int nsb;            // superblocks along K
@@ -204,16 +189,6 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 3-D box {18 x 8-byte elements of a block, rows, superblocks} of a weight matrix.
-__device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* tm, int row, int sb, uint64_t* bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(row), "r"(sb), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
 }
 
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
@@ -537,72 +512,19 @@ constexpr size_t gemv_smem() {
          (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
 }
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelExC(&cfg, fn, args);
-}
-
 template <bool GATEUP, int NT>
 cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                         cudaStream_t s) {
   using S = Shape<GATEUP, NT>;
   auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES, S::CPS>;
   constexpr size_t smem = gemv_smem<GATEUP, NT>();
-  static uint64_t attr_set = 0;  // one bit per device: the attribute is set per function and device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static uint64_t attr_set = 0;  // one bit per device
+  const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !(attr_set >> dev & 1)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set |= 1ull << dev;
-  }
   void* args[] = {const_cast<CUtensorMap*>(&t0), const_cast<CUtensorMap*>(&t1), const_cast<GemvParams*>(&P)};
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS / S::TPW * S::SLICES * 32), smem, s,
                     args);
 }
-
-// Weight matrix [rows][nsb blocks] as a 3-D tensor {18 x 8-byte elements of a
-// block, rows, blocks}; a box of box_rows rows x slices superblocks lands in
-// shared memory superblock-major, 144 bytes per row.
-bool weight_map(CUtensorMap* m, const void* w, int rows, int nsb, int box_rows, int slices) {
-  const cuuint64_t dims[3] = {(cuuint64_t)(BLK / 8), (cuuint64_t)rows, (cuuint64_t)nsb};
-  const cuuint64_t strides[2] = {(cuuint64_t)nsb * BLK, (cuuint64_t)BLK};
-  const cuuint32_t box[3] = {(cuuint32_t)(BLK / 8), (cuuint32_t)box_rows, (cuuint32_t)slices};
-  return tmap_encode_cached(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 3, w, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
-// Number of K-chunks: the most, up to max_nks, among those that minimise the longest CTA's
-// group steps. The cap bounds the partial-sum buffers (nks x m x rows floats).
-void choose_split(int ngroups, int nru, int grid, int max_nks, int* nks_out, int* gpc_out) {
-  int64_t best = INT64_MAX;
-  int best_nks = 1, best_gpc = ngroups;
-  for (int t = 1; t <= ngroups && t <= max_nks; ++t) {
-    const int gpc = (ngroups + t - 1) / t;
-    const int nks = (ngroups + gpc - 1) / gpc;
-    if (nks != t) continue;
-    const int64_t per_cta = ((int64_t)nks * nru + grid - 1) / grid;
-    const int64_t cost = per_cta * gpc;
-    if (cost <= best) {  // ties go to more chunks: one group per chunk lets warps keep their inputs
-      best = cost;
-      best_nks = nks;
-      best_gpc = gpc;
-    }
-  }
-  *nks_out = best_nks;
-  *gpc_out = best_gpc;
-}
-
-inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 }  // namespace
 
@@ -696,16 +618,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   if (e != cudaSuccess) return e;
 
   prof.before(4, s);  // the down-chunk sum (absent when K is not split)
-  if (p.nks2 > 1) {
-    const float* pp = p2;
-    int nks = p.nks2;
-    int64_t n = (int64_t)p.m * p.hidden;
-    float* yy = y;
-    void* args[] = {&pp, &nks, &n, &yy};
-    // small CTAs spread the sums over more SMs (more loads in flight)
-    e = launch_pdl(reinterpret_cast<const void*>(finish_down_kernel), dim3((unsigned)((n / 4 + 63) / 64)), dim3(64),
-                   0, s, args);
-  }
+  if (p.nks2 > 1) e = launch_finish_down(p2, p.nks2, (int64_t)p.m * p.hidden, y, s);
   prof.after(4, s);
   return e;
 }

@@ -34,6 +34,23 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
                           float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
 
+// ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8)
+struct DecodeQ8Plan {
+  int m, hidden, inter;
+  int mt;              // tokens the GEMV kernels are compiled for (1, 2, 4 or 8; >= m)
+  int nks1, kc1;       // gate/up K-chunks and superblock groups per chunk
+  int nks2, kc2;       // down K-chunks and superblock groups per chunk
+  int grid1, grid2;    // CTAs
+  size_t ws_bytes;     // workspace bytes
+  // workspace offsets (bytes): planar Q8_1 of x and of h, gate/up and down chunk sums
+  size_t off_xq, off_hq, off_p1, off_p2;
+};
+int decode_q8_tokens(int64_t m);
+bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodeQ8Plan* p);
+cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, const void* wg, const void* wu,
+                             const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
+                             const ProfileEvents& prof);
+
 // ---------------------------------------------------------------- prefill (m >= 9)
 struct PrefillPlan {
   int m, hidden, inter;

@@ -8,6 +8,7 @@
 // 64g+32+i).
 #include "common.cuh"
 #include "kernels.h"
+#include "q8_1.cuh"
 
 namespace q4k {
 
@@ -74,28 +75,6 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
     v[2 * i] = __uint_as_float(w[i] << 16);
     v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
-}
-
-__device__ __forceinline__ void q8_1_block8(const float v[8], int8_t q[8], float& d, float& s) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
-  d = nz ? __fdiv_rn(amax, 127.f) : 0.f;
-  const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
-  int sum = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float r = roundf(__fmul_rn(v[i], inv));
-    r = fminf(fmaxf(r, -127.f), 127.f);
-    q[i] = (int8_t)(int)r;
-    sum += (int)r;
-  }
-  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-  s = __fmul_rn(d, (float)sum);
 }
 
 template <typename T>
