@@ -35,7 +35,7 @@
 // activation bytes per token (64, plus two {d8, s8} pairs) are contiguous. At
 // the end of a unit the four lanes of a row are summed by shuffles and an owner
 // warp sums the SLICES partial dot products through shared memory; the chunks
-// are summed by K1b / K3 in a fixed order, so results are deterministic.
+// are summed by K1b / K3 in chunk order, so results are deterministic.
 #include <algorithm>
 #include <cmath>
 
@@ -67,10 +67,31 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
   return d;
 }
 
+// Shared memory of a CTA: the stage ring, the stage barriers, the unit-end
+// reduction slots, the abort flag and, for more than two tokens, one slot per
+// warp for the Q8_1 activations of its current superblock (per token 256 quant
+// bytes and 8 {d8, s8} pairs).
+template <bool GATEUP, int MT, int COMBOS, int TPW, int SLICES, int STAGES>
+struct Q8Smem {
+  static constexpr int WARPS = COMBOS / TPW * SLICES;
+  static constexpr int RU = GATEUP ? 16 : 16 * COMBOS;
+  static constexpr int BOX_BYTES = SLICES * RU * BLK;
+  static constexpr int STAGE_BYTES = (GATEUP ? 2 : 1) * BOX_BYTES;
+  static constexpr int PER_WARP = 8 * TPW * MT * 2;
+  static constexpr bool XCACHE = MT <= 2;  // activations kept in registers instead
+  static constexpr int XS_TOKEN = QK + 8 * 8;
+  static constexpr size_t OFF_BAR = (size_t)STAGES * STAGE_BYTES;
+  static constexpr size_t OFF_RED = OFF_BAR + 2 * STAGES * 8;
+  static constexpr size_t OFF_FLAG = OFF_RED + (size_t)2 * WARPS * PER_WARP * 4;
+  static constexpr size_t OFF_XS = (OFF_FLAG + 16 + 15) & ~(size_t)15;
+  static constexpr size_t BYTES = OFF_XS + (XCACHE ? 0 : (size_t)WARPS * MT * XS_TOKEN);
+};
+
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
 // COMBOS consecutive tiles of W_down); each warp takes TPW of them at one of the
-// SLICES superblocks. MT >= m tokens; the activations of up to two tokens stay
-// in registers while a warp's superblock does not change.
+// SLICES superblocks. MT >= m tokens; the activations of the warp's superblock
+// stay in registers (up to two tokens) or in the warp's shared-memory slot
+// while that superblock does not change.
 template <bool GATEUP, int MT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>
 __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     gemv_q8_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
@@ -84,11 +105,12 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   constexpr int BOX_BYTES = SLICES * RU * BLK;      // one box: [SLICES][RU rows][144 B]
   constexpr int STAGE_BYTES = MATS * BOX_BYTES;
   constexpr int PER_WARP = 8 * TPW * MT * 2;         // reduction slot: [8 g][TPW][MT][2 rows]
+  using L = Q8Smem<GATEUP, MT, COMBOS, TPW, SLICES, STAGES>;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* empty = full + STAGES;
-  float* red = reinterpret_cast<float*>(empty + STAGES);  // [2][WARPS][PER_WARP]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * WARPS * PER_WARP);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);  // [2][WARPS][PER_WARP]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_FLAG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   const int tgrp = warp % TG, slice = warp / TG;
@@ -179,10 +201,11 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   for (int t = 0; t < TPW; ++t)
 #pragma unroll
     for (int k = 0; k < MT; ++k) acc[t][k][0] = acc[t][k][1] = 0.f;
-  constexpr bool XCACHE = MT <= 2;
+  constexpr bool XCACHE = L::XCACHE;
   constexpr int XC = XCACHE ? MT : 1;
   uint4 xa[XC][4];  // activation words: sub-block 2 tig (xa[.][0..1]) and 2 tig + 1 (xa[.][2..3])
   float4 xd[XC];    // {d8, s8} of those two blocks
+  uint8_t* xs = smem + L::OFF_XS + (size_t)warp * MT * L::XS_TOKEN;  // this warp's slot (MT > 2)
   int csb = -1;
   auto load_x = [&](int tok, int sb, uint4 w[4], float4& d) {
     const int tt = min(tok, P.m - 1);  // padding tokens read a real token; their sums are never stored
@@ -236,13 +259,29 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           const uint32_t mnp = ((vm >> sM) & mL) | ((vm >> 10) & mH);
           scl[t][r] = (int)(scp & 0xFFFFu);
           sch[t][r] = (int)(scp >> 16);
-          mnl[t][r] = (float)(mnp & 0xFFFFu);
-          mnh[t][r] = (float)(mnp >> 16);
+          // small non-negative integers to float: 2^23 + v has v in its mantissa
+          mnl[t][r] = __uint_as_float(prmt(mnp, 0x4B000000u, 0x7440u)) - 8388608.f;
+          mnh[t][r] = __uint_as_float(prmt(mnp, 0x4B000000u, 0x7442u)) - 8388608.f;
         }
       }
       if (XCACHE && sb != csb) {
 #pragma unroll
         for (int k = 0; k < XC; ++k) load_x(k, sb, xa[k], xd[k]);
+        csb = sb;
+      }
+      if (!XCACHE && sb != csb) {
+        // copy the superblock's activations of every token into the slot, 16 bytes a lane
+        __syncwarp();
+        constexpr int CH = L::XS_TOKEN / 16;
+        for (int c = lane; c < MT * CH; c += 32) {
+          const int k = c / CH, j = c - k * CH;
+          const int tt = min(k, P.m - 1);
+          const uint4 v = j < QK / 16
+                              ? reinterpret_cast<const uint4*>(P.xq + (int64_t)tt * kq + (int64_t)sb * QK)[j]
+                              : reinterpret_cast<const uint4*>(P.xds + ((int64_t)tt * P.nsb + sb) * 4)[j - QK / 16];
+          reinterpret_cast<uint4*>(xs + k * L::XS_TOKEN)[j] = v;
+        }
+        __syncwarp();
         csb = sb;
       }
 #pragma unroll
@@ -254,7 +293,10 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           for (int i = 0; i < 4; ++i) xw[i] = xa[XCACHE ? k : 0][i];
           dsv = xd[XCACHE ? k : 0];
         } else {
-          load_x(k, sb, xw, dsv);
+          const uint4* xp = reinterpret_cast<const uint4*>(xs + k * L::XS_TOKEN + 64 * tig);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) xw[i] = xp[i];
+          dsv = reinterpret_cast<const float4*>(xs + k * L::XS_TOKEN + QK)[tig];
         }
         const uint32_t xl[8] = {xw[0].x, xw[0].y, xw[0].z, xw[0].w, xw[1].x, xw[1].y, xw[1].z, xw[1].w};
         const uint32_t xh[8] = {xw[2].x, xw[2].y, xw[2].z, xw[2].w, xw[3].x, xw[3].y, xw[3].z, xw[3].w};
@@ -270,7 +312,10 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
               il = dp4a_us(w[c] & 0x0F0F0F0Fu, xl[c], il);
               ih = dp4a_us(w[c] & 0xF0F0F0F0u, xh[c], ih);
             }
-            const float sm = fmaf((float)(il * scl[t][r]), dsv.x, (float)((ih >> 4) * sch[t][r]) * dsv.z);
+            // |I * scale| < 2^22: 1.5 * 2^23 + v holds v exactly in its mantissa
+            const float fl = __int_as_float(il * scl[t][r] + 0x4B400000) - 12582912.f;
+            const float fh = __int_as_float((ih >> 4) * sch[t][r] + 0x4B400000) - 12582912.f;
+            const float sm = fmaf(fl, dsv.x, fh * dsv.z);
             const float mn = fmaf(mnl[t][r], dsv.y, mnh[t][r] * dsv.w);
             acc[t][k][r] = fmaf(dd[t][r], sm, fmaf(-dm[t][r], mn, acc[t][k][r]));
           }
@@ -333,10 +378,10 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes. One or two tokens: two CTAs per SM of 8 warps, each warp two
-// tiles, two stages (K1: gate and up boxes of 16 rows x 8 superblocks; K2: one
-// box of 64 rows x 4 superblocks). Three to eight tokens: one CTA per SM, four
-// stages (more registers for the partial sums).
+// CTA shapes: 8 warps, each warp two tiles (K1: gate and up boxes of 16 rows x
+// 8 superblocks; K2: one box of 64 rows x 4 superblocks). One or two tokens:
+// two CTAs per SM, two stages. Three to eight tokens: one CTA per SM (registers
+// for the partial sums of every token), four stages.
 template <bool GATEUP, int MT> struct ShapeQ8;
 template <int MT> struct ShapeQ8<true, MT> {
   static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = MT <= 2 ? 2 : 4, CPS = MT <= 2 ? 2 : 1;
@@ -348,8 +393,7 @@ template <int MT> struct ShapeQ8<false, MT> {
 template <bool GATEUP, int MT>
 constexpr size_t gemv_q8_smem() {
   using S = ShapeQ8<GATEUP, MT>;
-  return (size_t)S::STAGES * S::COMBOS * 16 * S::SLICES * BLK + 2 * S::STAGES * 8 +
-         (size_t)2 * (S::COMBOS / S::TPW * S::SLICES) * 8 * S::TPW * MT * 2 * 4 + 16;
+  return Q8Smem<GATEUP, MT, S::COMBOS, S::TPW, S::SLICES, S::STAGES>::BYTES;
 }
 
 template <bool GATEUP, int MT>

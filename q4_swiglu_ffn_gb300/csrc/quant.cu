@@ -81,6 +81,7 @@ template <typename T>
 __global__ void q8_1_kernel(const T* __restrict__ x, int8_t* __restrict__ qs, float2* __restrict__ ds,
                             int64_t m, int64_t k) {
   // one thread per 8 values; 4 threads per Q8_1 block; rows of k values
+  pdl_launch_dependents();  // a dependent GEMV may start streaming its weights (it waits before reading q)
   const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t per_row = k / 8;
   const bool active = gid < m * per_row;
