@@ -15,6 +15,8 @@ What it computes (plain numpy, float64 unless the definition fixes float32):
                           gate/up and the activated vector re-quantized before down.
 * ``quantize_q4k``     -- deterministic min-max Q4_K weight quantizer.
 * ``q4k_q8_1_dot``     -- the closed form of one Q4_K x Q8_1 block dot product.
+* ``dequantize_q6k``   -- exact value of every weight of a GGML Q6_K block.
+* ``gemv_q6k``         -- y = W x over exact Q6_K weights (the LM-head GEMV).
 
 Pins (tests/test_oracle_*.py) tie every function to something other than
 itself: hand-built blocks whose values follow from the block definition,
@@ -30,3 +32,4 @@ from .q4k import (  # noqa: F401
     silu, ffn_decode, ffn_prefill, ffn_down_from_q8_1, gate_up_h,
     quantize_q4k, q4k_q8_1_dot,
 )
+from .q6k import Q6K_BLOCK_BYTES, q6k_fields, dequantize_q6k, gemv_q6k  # noqa: F401

@@ -59,3 +59,22 @@ def silu(z: float) -> float:
 
 def f32(v: float) -> float:
     return struct.unpack("<f", struct.pack("<f", v))[0]
+
+
+def q6k_weight(block: bytes, i: int) -> float:
+    """Value of weight i (0..255) of one 210-byte Q6_K block, as an exact float.
+
+    Written per byte and bit from the block description (ql[128] low nibbles,
+    qh[64] high 2-bit fields, 16 signed scales at byte 192, fp16 d at byte 208).
+    """
+    d = half_to_float(block[208], block[209])
+    h, r = divmod(i, 128)
+    s, l = divmod(r, 32)
+    byte = block[64 * h + l + 32 * (s % 2)]
+    nib = (byte & 0x0F) if s < 2 else (byte >> 4)
+    top = (block[128 + 32 * h + l] >> (2 * s)) & 3
+    q = nib + 16 * top
+    sc = block[192 + i // 16]
+    if sc >= 128:
+        sc -= 256
+    return d * sc * (q - 32)

@@ -96,6 +96,59 @@ def q4k_blocks(seed: int, stream: int, rows: int, cols: int,
     return raw.reshape(rows, cols // QK_K, BLOCK_BYTES)
 
 
+Q6K_BLOCK_BYTES = 210  # bytes per Q6_K block
+
+
+def q6k_blocks(seed: int, stream: int, rows: int, cols: int,
+               d_lo: float = 0.0005, d_hi: float = 0.002) -> np.ndarray:
+    """Random Q6_K weight matrix: uint8 array [rows, cols/256, 210].
+
+    Bytes 208-209 hold fp16 d (U[d_lo, d_hi] rounded to fp16); bytes 0-207
+    (the quant bits and the 16 signed 8-bit scales) are uniformly random, so
+    every 6-bit quant is uniform on 0..63 and every scale on -128..127.
+    """
+    assert cols % QK_K == 0
+    nb = rows * (cols // QK_K)
+    raw = random_bytes(seed, stream, nb * Q6K_BLOCK_BYTES).reshape(nb, Q6K_BLOCK_BYTES)
+    u = uniform(seed, stream + 100, nb)
+    dd = (d_lo + (d_hi - d_lo) * u).astype(np.float16)
+    raw[:, 208:210] = dd.view(np.uint8).reshape(nb, 2)
+    return raw.reshape(rows, cols // QK_K, Q6K_BLOCK_BYTES)
+
+
+@dataclasses.dataclass(frozen=True)
+class LMHeadConfig:
+    """A Q6_K GEMV workload: y [m, n] = x [m, k] . W[n, k]^T (an LM head)."""
+    index: int
+    name: str
+    n: int      # output rows (vocabulary)
+    k: int      # inputs (hidden)
+    m: int      # tokens
+
+    @property
+    def seed(self) -> int:
+        return 0x5EED0600 + self.index
+
+    def weight_bytes(self) -> int:
+        return self.n * self.k // QK_K * Q6K_BLOCK_BYTES
+
+
+# LLaMA-7B's output projection (vocabulary 32000, hidden 4096) at decode, and a small case
+LMHEADS = [
+    LMHeadConfig(0, "tiny-lmhead-q6k-n512-k256-m1", 512, 256, 1),
+    LMHeadConfig(1, "llama7b-lmhead-q6k-n32000-k4096-m1", 32000, 4096, 1),
+]
+
+
+def lmhead_weights(cfg: LMHeadConfig) -> np.ndarray:
+    return q6k_blocks(cfg.seed, S_WG, cfg.n, cfg.k)
+
+
+def lmhead_x(cfg: LMHeadConfig, m: int | None = None) -> np.ndarray:
+    m = cfg.m if m is None else m
+    return normal(cfg.seed, S_X, m * cfg.k).reshape(m, cfg.k).astype(np.float32)
+
+
 @dataclasses.dataclass(frozen=True)
 class Config:
     index: int
