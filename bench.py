@@ -50,6 +50,7 @@ def parse():
     ap.add_argument("--prefill-steps", type=int, default=120)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_1-activation decode leg")
+    ap.add_argument("--no-q6k", action="store_true", help="skip the Q6_K LM-head GEMV leg")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -276,6 +277,61 @@ def gpu_decode(args, rank, world, dist, path="f32"):
             "wbytes": wbytes, "xbytes": x_np.nbytes, "launches_per_step": launches, "pct": pct, "G": G}
 
 
+def gpu_q6k(args):
+    """The Q6_K LM-head GEMV (LLaMA-7B output projection, m = 1), graph-replayed like the decode."""
+    import torch
+    import workloads
+    import q4_swiglu_ffn_gb300 as q
+
+    c = workloads.LMHEADS[1]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wbytes = c.weight_bytes()
+    R = max(2, math.ceil(3 * L2_BYTES / wbytes))
+    base = workloads.lmhead_weights(c)
+    reps = [torch.from_numpy(base).to(dev) for _ in range(R)]
+    x = torch.from_numpy(workloads.lmhead_x(c)).to(dev)
+    y = torch.empty((c.m, c.n), dtype=torch.float32, device=dev)
+    ws = torch.empty(q.q6k_gemv_workspace_bytes(c.m, c.n, c.k), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+
+    def step(i):
+        q.q6k_gemv(x, reps[i % R], ws, y=y)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    G = R * max(1, 64 // R)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            step(i)
+    graph.replay()
+    torch.cuda.synchronize()
+    n_rep = max(3, math.ceil(args.steps / 4 / G))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_rep):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (n_rep * G)
+    P = 200
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(P)]
+    for ev in evs:
+        for e in ev:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(P):
+        q.q4k_set_profile_events(evs[i])
+        step(i)
+    q.q4k_set_profile_events(None)
+    torch.cuda.synchronize()
+    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(2)]
+    assert q.q4k_check_device_error() == 0
+    return {"cfg": c, "ms": ms, "K": n_rep * G, "kern_ms": kern_ms, "wbytes": wbytes, "R": R}
+
+
 def gpu_prefill(args):
     import torch
     import workloads
@@ -390,6 +446,10 @@ def main():
     if not args.no_q8 and rank == 0:
         r8 = gpu_decode(args, rank, 1, None, path="q8_1")
 
+    r6 = None
+    if not args.no_q6k and rank == 0:
+        r6 = gpu_q6k(args)
+
     pre = None
     if not args.no_prefill and rank == 0:
         pre = gpu_prefill(args)
@@ -446,6 +506,18 @@ def main():
                          "avg_launch_ms": k1q_ms},
             "gpu_launches": r8["launches_per_step"] * r8["K"],
             "clocks": r8["clocks"]}
+    if r6 is not None:
+        c6 = r6["cfg"]
+        ach6 = r6["wbytes"] / (r6["kern_ms"][1] * 1e-3) / 1e9
+        line["lmhead_q6k"] = {
+            "workload": c6.name, "value": r6["wbytes"] / (r6["ms"] * 1e-3) / 1e9, "unit": "GB/s",
+            "ms_per_step": r6["ms"], "steps": r6["K"], "dtype": "f16 (x as fp16 hi + lo), f32 accumulate",
+            "kernels_ms": dict(zip(["x_fragments", "q6k_gemv"], r6["kern_ms"])),
+            "roofline": {"kernel": "q6k_gemv_kernel", "bound": "hbm", "achieved": ach6, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach6 / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth",
+                         "algorithmic_bytes_per_launch": r6["wbytes"], "avg_launch_ms": r6["kern_ms"][1]},
+            "step_frac": (r6["wbytes"] / (r6["ms"] * 1e-3) / 1e9) / pk["hbm_gbs"],
+            "l2": f"rotating {r6['R']} weight replicas"}
     if pre is not None:
         c = pre["cfg"]
         gu_ops = 2 * c.m * c.hidden * c.inter * 2

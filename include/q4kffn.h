@@ -165,6 +165,35 @@ q4k_status ffn_q4k_swiglu_noalloc(const void* x, int64_t m, int64_t hidden, int6
                                   const void* W_gate, const void* W_up, const void* W_down,
                                   float* y, q4k_stream_t stream);
 
+/* ---- Q6_K GEMV (the LM head) ----
+ * Q6_K block (GGML block_q6_K, 256 weights in 210 bytes): ql[128] low 4 bits
+ * of the quants, qh[64] high 2 bits, 16 signed 8-bit sub-block scales, fp16 d.
+ * Weight i is d * scale[i / 16] * (q_i - 32); in half h (weights 128h..128h+127),
+ * weight 128h + 32s + l (s = 0..3, l = 0..31) takes its low 4 bits from the
+ * low (s < 2) or high (s >= 2) nibble of ql[64h + l + 32*(s % 2)] and its high 2
+ * bits from bits 2s..2s+1 of qh[32h + l]. */
+/* Bytes of a Q6_K matrix of `rows` rows of `cols` inputs: rows*(cols/256)*210
+ * (0 for an invalid shape). */
+size_t q6k_weight_bytes(int64_t rows, int64_t cols);
+/* Workspace bytes q6k_gemv needs (0 for a shape q6k_gemv rejects). */
+size_t q6k_gemv_workspace_bytes(int64_t m, int64_t n, int64_t k);
+/* y[t][r] = sum_c W[r][c] * x[t][c] for t < m, r < n: the GEMV of a Q6_K weight
+ * matrix W (n rows of k/256 blocks, row = output) with float32 or bf16
+ * activations x [m][k] (bf16 widened exactly), float32 output y [m][n].
+ * Source: realizar src/cuda/executor/q4k_gemv_cached_uses.rs,
+ * q6k_gemv_cached_async (the Q4_K GEMV's contract for Q6_K weights, used for the
+ * LM head). Shapes: 1 <= m <= 8, n a positive multiple of 16, k a multiple of
+ * 256 up to 8192 (else Q4K_ERR_SHAPE). x, W, y 16-byte aligned; the workspace
+ * caller-owned, 256-byte aligned, at least q6k_gemv_workspace_bytes(m, n, k)
+ * bytes, no initialisation needed, not shared by calls that overlap on the GPU.
+ * Repeated calls with the same buffers are replayed from a recorded CUDA graph. */
+q4k_status q6k_gemv(const void* x, q4k_dtype dtype, int64_t m, int64_t n, int64_t k,
+                    const void* W, float* y, void* workspace, size_t ws_bytes,
+                    q4k_stream_t stream);
+/* Test hook: dequantize a Q6_K matrix to float32 [rows][cols]; every value
+ * d*scale*(q-32) is exact in float32. */
+q4k_status q6k_dequantize(const void* q6k, int64_t rows, int64_t cols, float* out,
+                          q4k_stream_t stream);
 /* Workspace bytes ffn_q4k_swiglu_ex needs for this shape (0 for an invalid shape). */
 size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
 

@@ -38,6 +38,10 @@ _SIGS = {
     "ffn_q4k_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "ffn_q4k_workspace_h_q8_1_offset": (_sz, [_i64, _i64, _i64]),
     "q4k_dequantize": (_int, [_p, _i64, _i64, _p, _p]),
+    "q6k_weight_bytes": (_sz, [_i64, _i64]),
+    "q6k_gemv_workspace_bytes": (_sz, [_i64, _i64, _i64]),
+    "q6k_gemv": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _sz, _p]),
+    "q6k_dequantize": (_int, [_p, _i64, _i64, _p, _p]),
     "q4k_check_device_error": (_int, [_p]),
     "q4k_test_bounded_wait": (_int, [ctypes.c_uint64, _p]),
     "q4k_set_profile_events": (_int, [_p, _int]),
@@ -170,6 +174,35 @@ def q4k_dequantize(q, rows: int, cols: int, out=None, stream=None):
     if out is None:
         out = torch.empty((rows, cols), dtype=torch.float32, device=q.device)
     _check(lib.q4k_dequantize(_ptr(q), rows, cols, _ptr(out), _stream(stream)), "q4k_dequantize")
+    return out
+
+
+def q6k_weight_bytes(rows: int, cols: int) -> int:
+    return lib.q6k_weight_bytes(rows, cols)
+
+
+def q6k_gemv_workspace_bytes(m: int, n: int, k: int) -> int:
+    return lib.q6k_gemv_workspace_bytes(m, n, k)
+
+
+def q6k_gemv(x, W, workspace, y=None, stream=None):
+    """y [m, n] = x [m, k] . W^T for Q6_K blocks W (uint8 [n, k/256, 210]); x float32 or bf16."""
+    import torch
+    m, k = x.shape
+    n = W.shape[0]
+    if y is None:
+        y = torch.empty((m, n), dtype=torch.float32, device=x.device)
+    _check(lib.q6k_gemv(_ptr(x), _dtype_code(x), m, n, k, _ptr(W), _ptr(y), _ptr(workspace), workspace.numel(),
+                        _stream(stream)), "q6k_gemv")
+    return y
+
+
+def q6k_dequantize(q, rows: int, cols: int, out=None, stream=None):
+    """Test hook: Q6_K blocks -> float32 [rows, cols]."""
+    import torch
+    if out is None:
+        out = torch.empty((rows, cols), dtype=torch.float32, device=q.device)
+    _check(lib.q6k_dequantize(_ptr(q), rows, cols, _ptr(out), _stream(stream)), "q6k_dequantize")
     return out
 
 

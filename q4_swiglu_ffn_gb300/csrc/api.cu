@@ -105,7 +105,7 @@ size_t plan_bytes_q8(int64_t m, int64_t hidden, int64_t inter, int sms) {
 // directly.
 struct DecodeGraph {
   bool used = false;
-  int path = 0;  // 0: float32 activations, 1: Q8_1 activations
+  int path = 0;  // 0: float32 activations, 1: Q8_1 activations, 2: Q6_K GEMV (wg = W, hidden = k, inter = n)
   const void *x = nullptr, *wg = nullptr, *wu = nullptr, *wd = nullptr, *ws = nullptr;
   float* y = nullptr;
   int dtype = 0;
@@ -192,6 +192,17 @@ q4k_status run_decode_q8(const q4k::DecodeQ8Plan& p, const void* x, int dtype, c
   key.dtype = dtype, key.m = p.m, key.hidden = p.hidden, key.inter = p.inter;
   return run_graphed(key, s, [&](cudaStream_t st, const q4k::ProfileEvents& pr) {
     return q4k::launch_decode_q8(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, st, pr);
+  });
+}
+
+q4k_status run_q6k(const q4k::Q6Plan& p, const void* x, int dtype, const void* w, float* y, void* ws, DeviceState* d,
+                   cudaStream_t s) {
+  DecodeGraph key;
+  key.path = 2;
+  key.x = x, key.wg = w, key.ws = ws, key.y = y;
+  key.dtype = dtype, key.m = p.m, key.hidden = p.k, key.inter = p.n;
+  return run_graphed(key, s, [&](cudaStream_t st, const q4k::ProfileEvents& pr) {
+    return q4k::launch_q6k_gemv(p, x, dtype == Q4K_BF16, w, y, ws, d->err, st, pr);
   });
 }
 
@@ -332,6 +343,46 @@ size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter)
   }
   q4k::PrefillPlan p;
   return q4k::prefill_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
+}
+
+size_t q6k_weight_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || rows > MAX_DIM || !dim_ok(cols)) return 0;
+  return (size_t)rows * (size_t)(cols / q4k::QK) * 210;
+}
+
+size_t q6k_gemv_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+  DeviceState* d = nullptr;
+  if (device_state(&d) != Q4K_OK) return 0;
+  q4k::Q6Plan p;
+  return q4k::q6k_plan(m, n, k, d->sms, &p) ? p.ws_bytes : 0;
+}
+
+q4k_status q6k_gemv(const void* x, q4k_dtype dtype, int64_t m, int64_t n, int64_t k, const void* W, float* y,
+                    void* workspace, size_t ws_bytes, q4k_stream_t stream) {
+  if (!x || !W || !y || !workspace) return fail(Q4K_ERR_NULL);
+  if (dtype != Q4K_F32 && dtype != Q4K_BF16) return fail(Q4K_ERR_DTYPE);
+  if (m < 1 || m > 8 || n < 16 || n > MAX_DIM || n % 16 != 0 || !dim_ok(k) || k > 8192) return fail(Q4K_ERR_SHAPE);
+  if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  q4k::Q6Plan p;
+  if (!q4k::q6k_plan(m, n, k, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
+  if (ws_bytes < p.ws_bytes) return fail(Q4K_ERR_NOMEM);
+  st = run_q6k(p, x, dtype, W, y, workspace, d, (cudaStream_t)stream);
+  return st == Q4K_OK ? st : fail(st);
+}
+
+q4k_status q6k_dequantize(const void* q6k, int64_t rows, int64_t cols, float* out, q4k_stream_t stream) {
+  if (!q6k || !out) return fail(Q4K_ERR_NULL);
+  if (rows <= 0 || rows > MAX_DIM || !dim_ok(cols) || rows * cols > MAX_ELEMS) return fail(Q4K_ERR_SHAPE);
+  if (!aligned16(out)) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  if (q4k::launch_q6k_dequant(q6k, out, rows, cols, (cudaStream_t)stream) != cudaSuccess) return fail(Q4K_ERR_CUDA);
+  return Q4K_OK;
 }
 
 size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {

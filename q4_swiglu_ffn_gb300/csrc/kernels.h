@@ -51,6 +51,20 @@ cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, con
                              const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
                              const ProfileEvents& prof);
 
+// ---------------------------------------------------------------- Q6_K GEMV (m <= 8)
+struct Q6Plan {
+  int m, n, k;
+  int nt;              // n-tiles of 4 tokens (1 or 2)
+  int cps, grid;       // CTAs per SM and CTAs
+  size_t smem;         // dynamic shared memory per CTA
+  size_t ws_bytes;     // workspace bytes
+  size_t off_fx, off_sc;  // workspace offsets: B fragments of x and their 2^e factors
+};
+bool q6k_plan(int64_t m, int64_t n, int64_t k, int num_sms, Q6Plan* p);
+cudaError_t launch_q6k_gemv(const Q6Plan& p, const void* x, int bf16, const void* w, float* y, void* ws,
+                            uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
+cudaError_t launch_q6k_dequant(const void* w, float* out, int64_t rows, int64_t cols, cudaStream_t s);
+
 // ---------------------------------------------------------------- prefill (m >= 9)
 struct PrefillPlan {
   int m, hidden, inter;
