@@ -116,6 +116,85 @@ __device__ __forceinline__ float sbyte_f(uint32_t w, int b) {
   return __int_as_float((int)prmt(w, 0u, sel) + 0x4B400000) - 12582912.f;
 }
 
+// A 32-bit field of a block in shared memory. AL = 0: the field is 4-byte
+// aligned; AL = 1: it sits 2 bytes past a 4-byte boundary; AL = 2: either.
+template <int AL>
+__device__ __forceinline__ uint32_t ld_field(const uint8_t* p) {
+  if constexpr (AL == 0) {
+    return *reinterpret_cast<const uint32_t*>(p);
+  } else if constexpr (AL == 1) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p - 2);
+    return __funnelshift_r(w[0], w[1], 16);
+  } else {
+    return ld_u32_2(p);
+  }
+}
+
+// One superblock of a 16-row tile: rows g and g+8 start at r0 and r1. Adds to
+// acc[n][r] this superblock's dot products of rows g + 8r with the tokens of
+// token tile n (B: the superblock's B fragments, xsc: 2^e of this lane's token).
+template <int AL, int NT>
+__device__ __forceinline__ void q6k_superblock(const uint8_t* r0, const uint8_t* r1, int tig,
+                                               const uint2 (&B)[16][NT], const float (&xsc)[NT], float (&acc)[NT][2]) {
+  const uint8_t* blk[2] = {r0, r1};
+  float dd[2];
+  uint32_t scw[2][4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    dd[r] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk[r] + 208)));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) scw[r][q] = ld_field<AL>(blk[r] + 192 + 4 * q);
+  }
+  float sacc[NT][4];
+#pragma unroll
+  for (int n = 0; n < NT; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) sacc[n][c] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      uint32_t qhw[2], qlw[2][2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        qhw[r] = ld_field<AL>(blk[r] + 128 + 32 * h + 16 * bb + 4 * tig);
+#pragma unroll
+        for (int s1 = 0; s1 < 2; ++s1) qlw[r][s1] = ld_field<AL>(blk[r] + 64 * h + 32 * s1 + 16 * bb + 4 * tig);
+      }
+#pragma unroll
+      for (int sp = 0; sp < 4; ++sp) {
+        const int j = 8 * h + 2 * sp + bb;  // sub-block: weights 16j .. 16j+15
+        uint32_t A[2][2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint32_t qw = qlw[r][sp & 1];
+          const uint32_t nib = sp < 2 ? (qw & 0x0F0F0F0Fu) : ((qw >> 4) & 0x0F0F0F0Fu);
+          const uint32_t top = sp < 2 ? ((qhw[r] << (4 - 2 * sp)) & 0x30303030u)
+                                      : ((qhw[r] >> (2 * sp - 4)) & 0x30303030u);
+          const uint32_t q4 = nib | top;  // bytes: the 6-bit q of positions 4tig .. 4tig+3
+          // fp16 1024 + q, then - 1056: q - 32 exactly
+          A[r][0] = h2_as_u32(__hadd2(u32_as_h2(prmt(q4, 0x64646464u, 0x5140u)), u32_as_h2(0xE420E420u)));
+          A[r][1] = h2_as_u32(__hadd2(u32_as_h2(prmt(q4, 0x64646464u, 0x7362u)), u32_as_h2(0xE420E420u)));
+        }
+        const float s0 = sbyte_f(scw[0][j >> 2], j & 3), s1 = sbyte_f(scw[1][j >> 2], j & 3);
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          float d4[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816(d4, A[0][0], A[1][0], A[0][1], A[1][1], B[j][n].x, B[j][n].y);
+          sacc[n][0] = fmaf(d4[0], s0, sacc[n][0]);
+          sacc[n][1] = fmaf(d4[1], s0, sacc[n][1]);
+          sacc[n][2] = fmaf(d4[2], s1, sacc[n][2]);
+          sacc[n][3] = fmaf(d4[3], s1, sacc[n][3]);
+        }
+      }
+    }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    acc[n][0] = fmaf(sacc[n][0] + sacc[n][1], dd[0] * xsc[n], acc[n][0]);
+    acc[n][1] = fmaf(sacc[n][2] + sacc[n][3], dd[1] * xsc[n], acc[n][1]);
+  }
+}
+
 struct Q6Params {
   const uint8_t* w;  // [n][nsb][210]
   int n, nsb, m, nt;
@@ -239,66 +318,19 @@ __global__ void __launch_bounds__(Q6_WARPS * 32, CPS) q6k_gemv_kernel(const Q6Pa
 #pragma unroll
             for (int n = 0; n < NT; ++n) xl[n] = P.in.sc[(int64_t)sb * 8 + 4 * n + tig];
           }
-          const uint8_t* blk[2];
-          blk[0] = st + (size_t)g * RB + (size_t)sb * Q6_BLK;
-          blk[1] = blk[0] + (size_t)8 * RB;
-          float dd[2];
-          uint32_t scw[2][4];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            dd[r] = __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk[r] + 208)));
-#pragma unroll
-            for (int q = 0; q < 4; ++q) scw[r][q] = ld_u32_2(blk[r] + 192 + 4 * q);
-          }
-          float sacc[NT][4];
-#pragma unroll
-          for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) sacc[n][c] = 0.f;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int bb = 0; bb < 2; ++bb) {
-              uint32_t qhw[2], qlw[2][2];
-#pragma unroll
-              for (int r = 0; r < 2; ++r) {
-                qhw[r] = ld_u32_2(blk[r] + 128 + 32 * h + 16 * bb + 4 * tig);
-#pragma unroll
-                for (int s1 = 0; s1 < 2; ++s1) qlw[r][s1] = ld_u32_2(blk[r] + 64 * h + 32 * s1 + 16 * bb + 4 * tig);
-              }
-#pragma unroll
-              for (int sp = 0; sp < 4; ++sp) {
-                const int j = 8 * h + 2 * sp + bb;  // sub-block: weights 16j .. 16j+15
-                uint32_t A[2][2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                  const uint32_t qw = qlw[r][sp & 1];
-                  const uint32_t nib = sp < 2 ? (qw & 0x0F0F0F0Fu) : ((qw >> 4) & 0x0F0F0F0Fu);
-                  const uint32_t top = sp < 2 ? ((qhw[r] << (4 - 2 * sp)) & 0x30303030u)
-                                              : ((qhw[r] >> (2 * sp - 4)) & 0x30303030u);
-                  const uint32_t q4 = nib | top;  // bytes: the 6-bit q of positions 4tig .. 4tig+3
-                  // fp16 1024 + q, then - 1056: q - 32 exactly
-                  A[r][0] = h2_as_u32(__hadd2(u32_as_h2(prmt(q4, 0x64646464u, 0x5140u)), u32_as_h2(0xE420E420u)));
-                  A[r][1] = h2_as_u32(__hadd2(u32_as_h2(prmt(q4, 0x64646464u, 0x7362u)), u32_as_h2(0xE420E420u)));
-                }
-                const float s0 = sbyte_f(scw[0][j >> 2], j & 3), s1 = sbyte_f(scw[1][j >> 2], j & 3);
-#pragma unroll
-                for (int n = 0; n < NT; ++n) {
-                  float d4[4] = {0.f, 0.f, 0.f, 0.f};
-                  const uint2 b = SBW > 0 ? bq[i][j][n] : bl[j][n];
-                  mma16816(d4, A[0][0], A[1][0], A[0][1], A[1][1], b.x, b.y);
-                  sacc[n][0] = fmaf(d4[0], s0, sacc[n][0]);
-                  sacc[n][1] = fmaf(d4[1], s0, sacc[n][1]);
-                  sacc[n][2] = fmaf(d4[2], s1, sacc[n][2]);
-                  sacc[n][3] = fmaf(d4[3], s1, sacc[n][3]);
-                }
-              }
-            }
-#pragma unroll
-          for (int n = 0; n < NT; ++n) {
-            const float x2 = SBW > 0 ? xs[i][n] : xl[n];
-            acc[n][0] = fmaf(sacc[n][0] + sacc[n][1], dd[0] * x2, acc[n][0]);
-            acc[n][1] = fmaf(sacc[n][2] + sacc[n][3], dd[1] * x2, acc[n][1]);
+          const uint8_t* r0 = st + (size_t)g * RB + (size_t)sb * Q6_BLK;
+          const uint8_t* r1 = r0 + (size_t)8 * RB;
+          // With an even number of blocks per row, a block's 2-byte offset from a 4-byte
+          // boundary depends only on its index, so it is the same for the whole warp.
+          const int mode = (RB & 3) ? 2 : (sb & 1);
+          if constexpr (SBW > 0) {
+            if (mode == 0) q6k_superblock<0, NT>(r0, r1, tig, bq[i], xs[i], acc);
+            else if (mode == 1) q6k_superblock<1, NT>(r0, r1, tig, bq[i], xs[i], acc);
+            else q6k_superblock<2, NT>(r0, r1, tig, bq[i], xs[i], acc);
+          } else {
+            if (mode == 0) q6k_superblock<0, NT>(r0, r1, tig, bl, xl, acc);
+            else if (mode == 1) q6k_superblock<1, NT>(r0, r1, tig, bl, xl, acc);
+            else q6k_superblock<2, NT>(r0, r1, tig, bl, xl, acc);
           }
         }
       }
