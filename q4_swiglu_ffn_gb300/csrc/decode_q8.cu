@@ -68,9 +68,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 }
 
 // Shared memory of a CTA: the stage ring, the stage barriers, the unit-end
-// reduction slots, the abort flag and, for more than two tokens, one slot per
-// warp for the Q8_1 activations of its current superblock (per token 256 quant
-// bytes and 8 {d8, s8} pairs).
+// reduction slots and the abort flag.
 template <bool GATEUP, int MT, int COMBOS, int TPW, int SLICES, int STAGES>
 struct Q8Smem {
   static constexpr int WARPS = COMBOS / TPW * SLICES;
@@ -78,20 +76,28 @@ struct Q8Smem {
   static constexpr int BOX_BYTES = SLICES * RU * BLK;
   static constexpr int STAGE_BYTES = (GATEUP ? 2 : 1) * BOX_BYTES;
   static constexpr int PER_WARP = 8 * TPW * MT * 2;
-  static constexpr bool XCACHE = MT <= 2;  // activations kept in registers instead
-  static constexpr int XS_TOKEN = QK + 8 * 8;
   static constexpr size_t OFF_BAR = (size_t)STAGES * STAGE_BYTES;
   static constexpr size_t OFF_RED = OFF_BAR + 2 * STAGES * 8;
   static constexpr size_t OFF_FLAG = OFF_RED + (size_t)2 * WARPS * PER_WARP * 4;
-  static constexpr size_t OFF_XS = (OFF_FLAG + 16 + 15) & ~(size_t)15;
-  static constexpr size_t BYTES = OFF_XS + (XCACHE ? 0 : (size_t)WARPS * MT * XS_TOKEN);
+  static constexpr size_t BYTES = OFF_FLAG + 16;
 };
+
+// m16n8k32 integer MMA: 4-bit quants as u8 (A), Q8_1 quants as s8 (B), int32 sums.
+__device__ __forceinline__ void mma_u8s8(int c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
 
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
 // COMBOS consecutive tiles of W_down); each warp takes TPW of them at one of the
-// SLICES superblocks. MT >= m tokens; the activations of the warp's superblock
-// stay in registers (up to two tokens) or in the warp's shared-memory slot
-// while that superblock does not change.
+// SLICES superblocks. MT >= m tokens. One or two tokens: dp4a, with the
+// activations of the warp's superblock in registers. Three to eight tokens:
+// mma.sync m16n8k32 (u8 weights x s8 activations, the 8 columns are the tokens),
+// one MMA per 32-weight sub-block and 16-row tile; a lane holds its column's
+// (token g's) activation words and the {d8, s8} of its two result columns.
 template <bool GATEUP, int MT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>
 __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     gemv_q8_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
@@ -201,11 +207,15 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   for (int t = 0; t < TPW; ++t)
 #pragma unroll
     for (int k = 0; k < MT; ++k) acc[t][k][0] = acc[t][k][1] = 0.f;
-  constexpr bool XCACHE = L::XCACHE;
-  constexpr int XC = XCACHE ? MT : 1;
-  uint4 xa[XC][4];  // activation words: sub-block 2 tig (xa[.][0..1]) and 2 tig + 1 (xa[.][2..3])
-  float4 xd[XC];    // {d8, s8} of those two blocks
-  uint8_t* xs = smem + L::OFF_XS + (size_t)warp * MT * L::XS_TOKEN;  // this warp's slot (MT > 2)
+  constexpr bool MMA = MT > 2;
+  constexpr int XC = MMA ? 1 : MT;
+  uint4 xa[XC][4];  // dp4a: activation words of sub-block 2 tig (xa[.][0..1]) and 2 tig + 1 (xa[.][2..3])
+  float4 xd[XC];    // dp4a: {d8, s8} of those two blocks
+  uint32_t bx[MMA ? 8 : 1][2];  // MMA: token g's words at positions 4tig.. and 16+4tig.. of sub-block j
+  float2 dx[MMA ? 2 : 1][8];    // MMA: {d8, s8} of tokens 2tig and 2tig+1, sub-block j
+  float accm[MMA ? TPW : 1][2][2];  // MMA: rows g, g+8 x tokens 2tig, 2tig+1
+#pragma unroll
+  for (int t = 0; t < (MMA ? TPW : 1); ++t) accm[t][0][0] = accm[t][0][1] = accm[t][1][0] = accm[t][1][1] = 0.f;
   int csb = -1;
   auto load_x = [&](int tok, int sb, uint4 w[4], float4& d) {
     const int tt = min(tok, P.m - 1);  // padding tokens read a real token; their sums are never stored
@@ -235,7 +245,75 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     }
     const int sb = cw.g * SLICES + slice;
     const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
-    if (!failed && sb < chunk_end) {
+    if constexpr (MMA) {
+      if (!failed && sb < chunk_end) {
+        // ---------------------------------------- TPW 16-row tiles of one superblock, 8 token columns
+        if (sb != csb) {
+          const uint8_t* xp = P.xq + (int64_t)min(g, P.m - 1) * kq + (int64_t)sb * QK + 4 * tig;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            bx[j][0] = *reinterpret_cast<const uint32_t*>(xp + 32 * j);
+            bx[j][1] = *reinterpret_cast<const uint32_t*>(xp + 32 * j + 16);
+          }
+          const float2* ds2 = reinterpret_cast<const float2*>(P.xds);
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int64_t tc = min(2 * tig + c, P.m - 1);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dx[c][j] = ds2[(tc * P.nsb + sb) * 8 + j];
+          }
+          csb = sb;
+        }
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+          const int cb = tgrp * TPW + t;
+          const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
+                                                                   : (slice * RU + cb * ROWS) * BLK);
+          uint32_t wl[2][4], wh[2][4], sw[2][3];
+          float dd[2], dm[2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const uint8_t* rb = base + (g + 8 * r) * BLK;
+            const uint4 hd = *reinterpret_cast<const uint4*>(rb);
+            const float2 dpair = __half22float2(u32_as_h2(hd.x));
+            dd[r] = dpair.x;
+            dm[r] = dpair.y;
+#pragma unroll
+            for (int G = 0; G < 4; ++G) {  // quant bytes 4tig.. and 16+4tig.. of group G
+              wl[r][G] = *reinterpret_cast<const uint32_t*>(rb + 16 + 32 * G + 4 * tig);
+              wh[r][G] = *reinterpret_cast<const uint32_t*>(rb + 32 + 32 * G + 4 * tig);
+            }
+            sw[r][0] = hd.y, sw[r][1] = hd.z, sw[r][2] = hd.w;
+          }
+          float sm[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, mn[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t mask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;  // sub-block 2G+1: 16 q in place
+            const int G = j >> 1;
+            int c4[4];
+            mma_u8s8(c4, wl[0][G] & mask, wl[1][G] & mask, wh[0][G] & mask, wh[1][G] & mask, bx[j][0], bx[j][1]);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              uint32_t sc, mq;
+              scale_min(sw[r][0], sw[r][1], sw[r][2], j, sc, mq);
+              const float mf = __uint_as_float(0x4B000000u | mq) - 8388608.f;
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int v = (j & 1) ? (c4[2 * r + c] >> 4) : c4[2 * r + c];  // exact: the sum is 16 * I
+                // |I * scale| < 2^22: 1.5 * 2^23 + v holds v exactly in its mantissa
+                const float f = __int_as_float(v * (int)sc + 0x4B400000) - 12582912.f;
+                sm[r][c] = fmaf(f, dx[c][j].x, sm[r][c]);
+                mn[r][c] = fmaf(mf, dx[c][j].y, mn[r][c]);
+              }
+            }
+          }
+#pragma unroll
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) accm[t][r][c] = fmaf(dd[r], sm[r][c], fmaf(-dm[r], mn[r][c], accm[t][r][c]));
+        }
+      }
+    } else if (!failed && sb < chunk_end) {
       // ------------------------------------------ TPW 16-row tiles of one superblock
       uint4 q0[TPW][2], q1[TPW][2];
       int scl[TPW][2], sch[TPW][2];
@@ -264,40 +342,17 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           mnh[t][r] = __uint_as_float(prmt(mnp, 0x4B000000u, 0x7442u)) - 8388608.f;
         }
       }
-      if (XCACHE && sb != csb) {
+      if (sb != csb) {
 #pragma unroll
         for (int k = 0; k < XC; ++k) load_x(k, sb, xa[k], xd[k]);
-        csb = sb;
-      }
-      if (!XCACHE && sb != csb) {
-        // copy the superblock's activations of every token into the slot, 16 bytes a lane
-        __syncwarp();
-        constexpr int CH = L::XS_TOKEN / 16;
-        for (int c = lane; c < MT * CH; c += 32) {
-          const int k = c / CH, j = c - k * CH;
-          const int tt = min(k, P.m - 1);
-          const uint4 v = j < QK / 16
-                              ? reinterpret_cast<const uint4*>(P.xq + (int64_t)tt * kq + (int64_t)sb * QK)[j]
-                              : reinterpret_cast<const uint4*>(P.xds + ((int64_t)tt * P.nsb + sb) * 4)[j - QK / 16];
-          reinterpret_cast<uint4*>(xs + k * L::XS_TOKEN)[j] = v;
-        }
-        __syncwarp();
         csb = sb;
       }
 #pragma unroll
       for (int k = 0; k < MT; ++k) {
         uint4 xw[4];
-        float4 dsv;
-        if (XCACHE) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) xw[i] = xa[XCACHE ? k : 0][i];
-          dsv = xd[XCACHE ? k : 0];
-        } else {
-          const uint4* xp = reinterpret_cast<const uint4*>(xs + k * L::XS_TOKEN + 64 * tig);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) xw[i] = xp[i];
-          dsv = reinterpret_cast<const float4*>(xs + k * L::XS_TOKEN + QK)[tig];
-        }
+        for (int i = 0; i < 4; ++i) xw[i] = xa[MMA ? 0 : k][i];
+        const float4 dsv = xd[MMA ? 0 : k];
         const uint32_t xl[8] = {xw[0].x, xw[0].y, xw[0].z, xw[0].w, xw[1].x, xw[1].y, xw[1].z, xw[1].w};
         const uint32_t xh[8] = {xw[2].x, xw[2].y, xw[2].z, xw[2].w, xw[3].x, xw[3].y, xw[3].z, xw[3].w};
 #pragma unroll
@@ -329,17 +384,29 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       // the four lanes of a row hold different sub-blocks: sum them; lane tig
       // then writes the tokens congruent to tig mod 4
       float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * PER_WARP + g * TPW * MT * 2;
+      if constexpr (MMA) {
+        // lane tig holds tokens 2tig and 2tig+1 of its rows
 #pragma unroll
-      for (int t = 0; t < TPW; ++t)
+        for (int t = 0; t < TPW; ++t)
 #pragma unroll
-        for (int k = 0; k < MT; ++k)
+          for (int c = 0; c < 2; ++c)
+            if (2 * tig + c < MT) {
+              slot[(t * MT + 2 * tig + c) * 2 + 0] = accm[t][0][c];
+              slot[(t * MT + 2 * tig + c) * 2 + 1] = accm[t][1][c];
+            }
+      } else {
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            float v = acc[t][k][r];
-            v += __shfl_xor_sync(0xffffffffu, v, 1);
-            v += __shfl_xor_sync(0xffffffffu, v, 2);
-            if ((k & 3) == tig) slot[(t * MT + k) * 2 + r] = v;
-          }
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int k = 0; k < MT; ++k)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              float v = acc[t][k][r];
+              v += __shfl_xor_sync(0xffffffffu, v, 1);
+              v += __shfl_xor_sync(0xffffffffu, v, 2);
+              if ((k & 3) == tig) slot[(t * MT + k) * 2 + r] = v;
+            }
+      }
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
       if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
         // owner: sum the SLICES partial dot products of every tile and store this chunk's sums
@@ -367,6 +434,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int k = 0; k < MT; ++k) acc[t][k][0] = acc[t][k][1] = 0.f;
+#pragma unroll
+      for (int t = 0; t < (MMA ? TPW : 1); ++t) accm[t][0][0] = accm[t][0][1] = accm[t][1][0] = accm[t][1][1] = 0.f;
       ++nunit;
       walk_next(cw);
     }
@@ -379,15 +448,14 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 }
 
 // CTA shapes: 8 warps, each warp two tiles (K1: gate and up boxes of 16 rows x
-// 8 superblocks; K2: one box of 64 rows x 4 superblocks). One or two tokens:
-// two CTAs per SM, two stages. Three to eight tokens: one CTA per SM (registers
-// for the partial sums of every token), four stages.
+// 8 superblocks; K2: one box of 64 rows x 4 superblocks), two CTAs per SM, two
+// stages.
 template <bool GATEUP, int MT> struct ShapeQ8;
 template <int MT> struct ShapeQ8<true, MT> {
-  static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = MT <= 2 ? 2 : 4, CPS = MT <= 2 ? 2 : 1;
+  static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2;
 };
 template <int MT> struct ShapeQ8<false, MT> {
-  static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = MT <= 2 ? 2 : 4, CPS = MT <= 2 ? 2 : 1;
+  static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2;
 };
 
 template <bool GATEUP, int MT>
