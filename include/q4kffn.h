@@ -17,6 +17,13 @@
  * Conventions for every entry point
  *   - Pointers are DEVICE pointers owned by the caller unless a comment says
  *     otherwise; the library never frees them. They must be 16-byte aligned.
+ *   - For ffn_q4k_swiglu, ffn_q4k_swiglu_ex, ffn_q4k_swiglu_q8_1 and q6k_gemv,
+ *     x and y may also be page-locked host memory mapped into the device's
+ *     address space (cudaHostAlloc / cudaHostRegister, which map by default
+ *     under unified addressing). GB300's host memory is coherent over
+ *     NVLink-C2C, so the kernels then read x and write y across the link
+ *     directly, with no separate copy. Other host memory (pageable, or without
+ *     a device mapping) returns Q4K_ERR_MEMORY before anything is launched.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and the call returns without synchronising.
  *   - Argument errors are detected on the host before anything is launched and
@@ -55,7 +62,8 @@ typedef enum {
   Q4K_ERR_ARCH = 6,      /* current device is not compute capability 10.3              */
   Q4K_ERR_TIMEOUT = 7,   /* a bounded device wait ran out (reported after the fact)    */
   Q4K_ERR_NOMEM = 8,     /* workspace allocation failed or caller workspace too small  */
-  Q4K_ERR_RANGE = 9      /* weight quantizer: a block scale does not fit in fp16       */
+  Q4K_ERR_RANGE = 9,     /* weight quantizer: a block scale does not fit in fp16       */
+  Q4K_ERR_MEMORY = 10    /* x or y is neither device memory nor mapped pinned host memory */
 } q4k_status;
 
 typedef enum { Q4K_F32 = 0, Q4K_BF16 = 1 } q4k_dtype;

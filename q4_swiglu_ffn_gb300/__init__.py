@@ -16,7 +16,8 @@ LIB_PATH = os.path.join(_HERE, "libq4kffn.so")
 
 Q4K_F32, Q4K_BF16 = 0, 1
 STATUS = {0: "Q4K_OK", 1: "Q4K_ERR_NULL", 2: "Q4K_ERR_SHAPE", 3: "Q4K_ERR_ALIGN", 4: "Q4K_ERR_DTYPE",
-          5: "Q4K_ERR_CUDA", 6: "Q4K_ERR_ARCH", 7: "Q4K_ERR_TIMEOUT", 8: "Q4K_ERR_NOMEM", 9: "Q4K_ERR_RANGE"}
+          5: "Q4K_ERR_CUDA", 6: "Q4K_ERR_ARCH", 7: "Q4K_ERR_TIMEOUT", 8: "Q4K_ERR_NOMEM", 9: "Q4K_ERR_RANGE",
+          10: "Q4K_ERR_MEMORY"}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python q4_swiglu_ffn_gb300/build.py`")

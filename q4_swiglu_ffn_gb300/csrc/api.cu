@@ -79,6 +79,37 @@ q4k_status check_ffn_args(const void* x, int dtype, int64_t m, int64_t hidden, i
 
 bool is_decode(int64_t m) { return m <= 8; }
 
+// x and y may be device (or managed) memory, used as is, or page-locked host
+// memory mapped into the device's address space: on GB300 the host memory is
+// coherent over NVLink-C2C, so the kernels then read x and write y across the
+// link with no separate copy. Host memory without a device mapping (pageable,
+// or registered without one) is refused, so no kernel touches an address the
+// device cannot reach.
+q4k_status resolve_io(const void* p, const void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return Q4K_ERR_MEMORY;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *out = p;
+    return Q4K_OK;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+    *out = a.devicePointer;
+    return Q4K_OK;
+  }
+  return Q4K_ERR_MEMORY;
+}
+
+q4k_status resolve_xy(const void** x, float** y) {
+  const void* yy = *y;
+  q4k_status st = resolve_io(*x, x);
+  if (st == Q4K_OK) st = resolve_io(yy, &yy);
+  *y = const_cast<float*>(static_cast<const float*>(yy));
+  return st;
+}
+
 size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
   if (is_decode(m)) {
     q4k::DecodePlan p;
@@ -271,6 +302,8 @@ q4k_status ffn_q4k_swiglu(const void* x, int64_t m, int64_t hidden, int64_t inte
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != Q4K_OK) return fail(st);
+  st = resolve_xy(&x, &y);
+  if (st != Q4K_OK) return fail(st);
   std::lock_guard<std::mutex> lk(d->mu);
   const size_t need = plan_bytes(m, hidden, inter, d->sms);
   if (need == 0) return fail(Q4K_ERR_SHAPE);
@@ -296,6 +329,8 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
   DeviceState* d = nullptr;
   st = device_state(&d);
   if (st != Q4K_OK) return fail(st);
+  st = resolve_xy(&x, &y);
+  if (st != Q4K_OK) return fail(st);
   const size_t need = plan_bytes(m, hidden, inter, d->sms);
   if (need == 0) return fail(Q4K_ERR_SHAPE);
   if (ws_bytes < need) return fail(Q4K_ERR_NOMEM);
@@ -312,6 +347,8 @@ q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4K_ERR_ALIGN);
   DeviceState* d = nullptr;
   st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  st = resolve_xy(&x, &y);
   if (st != Q4K_OK) return fail(st);
   const size_t need = plan_bytes_q8(m, hidden, inter, d->sms);
   if (need == 0) return fail(Q4K_ERR_SHAPE);
@@ -366,6 +403,8 @@ q4k_status q6k_gemv(const void* x, q4k_dtype dtype, int64_t m, int64_t n, int64_
     return fail(Q4K_ERR_ALIGN);
   DeviceState* d = nullptr;
   q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  st = resolve_xy(&x, &y);
   if (st != Q4K_OK) return fail(st);
   q4k::Q6Plan p;
   if (!q4k::q6k_plan(m, n, k, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
@@ -469,6 +508,7 @@ const char* q4k_status_string(q4k_status s) {
     case Q4K_ERR_TIMEOUT: return "bounded device wait timed out";
     case Q4K_ERR_NOMEM: return "workspace allocation failed or too small";
     case Q4K_ERR_RANGE: return "quantized scale outside the fp16 range";
+    case Q4K_ERR_MEMORY: return "pointer is neither device memory nor mapped page-locked host memory";
   }
   return "unknown status";
 }

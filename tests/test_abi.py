@@ -76,6 +76,6 @@ def test_argument_errors_before_any_launch(lib):
 
 def test_status_strings(lib):
     lib.q4k_status_string.restype = ctypes.c_char_p
-    for s in range(10):
+    for s in range(11):
         assert lib.q4k_status_string(s)
     assert b"unknown" in lib.q4k_status_string(99)
