@@ -6,6 +6,7 @@
 // errors returned before anything is launched (realizar
 // q4k_gemv_cached_uses.rs, q4k_gemv_indexed_async: refuse a null weight
 // pointer before launch; libmir micro_moe.rs: checked size arithmetic).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -77,7 +78,15 @@ q4k_status check_ffn_args(const void* x, int dtype, int64_t m, int64_t hidden, i
   return Q4K_OK;
 }
 
-bool is_decode(int64_t m) { return m <= 8; }
+// Up to DECODE_MAX tokens the call runs the decode kernels, in passes of at most
+// DECODE_CHUNK tokens (their token tiles hold 8): one GEMV pass streams all the
+// weights in about the time of a full-tile prefill GEMM's first wave, so passes
+// win while there are at most four of them (m <= 32 on the workloads measured).
+// From 33 tokens on the prefill GEMM runs.
+constexpr int64_t DECODE_CHUNK = 8;
+constexpr int64_t DECODE_MAX = 32;
+bool is_decode(int64_t m) { return m <= DECODE_MAX; }
+int64_t last_chunk(int64_t m) { return m - DECODE_CHUNK * ((m - 1) / DECODE_CHUNK); }
 
 // x and y may be device (or managed) memory, used as is, or page-locked host
 // memory mapped into the device's address space: on GB300 the host memory is
@@ -112,8 +121,11 @@ q4k_status resolve_xy(const void** x, float** y) {
 
 size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
   if (is_decode(m)) {
-    q4k::DecodePlan p;
-    return q4k::decode_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
+    q4k::DecodePlan a, b;
+    if (!q4k::decode_plan(std::min(m, DECODE_CHUNK), hidden, inter, sms, &a) ||
+        !q4k::decode_plan(last_chunk(m), hidden, inter, sms, &b))
+      return 0;
+    return std::max(a.ws_bytes, b.ws_bytes);
   }
   q4k::PrefillPlan p;
   return q4k::prefill_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
@@ -121,8 +133,11 @@ size_t plan_bytes(int64_t m, int64_t hidden, int64_t inter, int sms) {
 
 size_t plan_bytes_q8(int64_t m, int64_t hidden, int64_t inter, int sms) {
   if (is_decode(m)) {
-    q4k::DecodeQ8Plan p;
-    return q4k::decode_q8_plan(m, hidden, inter, sms, &p) ? p.ws_bytes : 0;
+    q4k::DecodeQ8Plan a, b;
+    if (!q4k::decode_q8_plan(std::min(m, DECODE_CHUNK), hidden, inter, sms, &a) ||
+        !q4k::decode_q8_plan(last_chunk(m), hidden, inter, sms, &b))
+      return 0;
+    return std::max(a.ws_bytes, b.ws_bytes);
   }
   return plan_bytes(m, hidden, inter, sms);
 }
@@ -241,9 +256,15 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
                    const void* wu, const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
   cudaError_t e;
   if (is_decode(m)) {
-    q4k::DecodePlan p;
-    if (!q4k::decode_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
-    return run_decode(p, x, dtype, wg, wu, wd, y, ws, d, s);
+    const int64_t xrow = hidden * (dtype == Q4K_BF16 ? 2 : 4);  // bytes of one token of x
+    for (int64_t t0 = 0; t0 < m; t0 += DECODE_CHUNK) {
+      q4k::DecodePlan p;
+      if (!q4k::decode_plan(std::min(DECODE_CHUNK, m - t0), hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
+      const q4k_status st = run_decode(p, static_cast<const uint8_t*>(x) + t0 * xrow, dtype, wg, wu, wd,
+                                       y + t0 * hidden, ws, d, s);
+      if (st != Q4K_OK) return st;
+    }
+    return Q4K_OK;
   } else {
     q4k::PrefillPlan p;
     if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
@@ -357,10 +378,15 @@ q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_
     st = run_ffn(x, dtype, m, hidden, inter, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
     return st == Q4K_OK ? st : fail(st);
   }
-  q4k::DecodeQ8Plan p;
-  if (!q4k::decode_q8_plan(m, hidden, inter, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
-  st = run_decode_q8(p, x, dtype, W_gate, W_up, W_down, y, workspace, d, (cudaStream_t)stream);
-  return st == Q4K_OK ? st : fail(st);
+  const int64_t xrow = hidden * (dtype == Q4K_BF16 ? 2 : 4);  // bytes of one token of x
+  for (int64_t t0 = 0; t0 < m; t0 += DECODE_CHUNK) {
+    q4k::DecodeQ8Plan p;
+    if (!q4k::decode_q8_plan(std::min(DECODE_CHUNK, m - t0), hidden, inter, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
+    st = run_decode_q8(p, static_cast<const uint8_t*>(x) + t0 * xrow, dtype, W_gate, W_up, W_down, y + t0 * hidden,
+                       workspace, d, (cudaStream_t)stream);
+    if (st != Q4K_OK) return fail(st);
+  }
+  return Q4K_OK;
 }
 
 size_t ffn_q4k_q8_1_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {
@@ -375,8 +401,8 @@ size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter)
   DeviceState* d = nullptr;
   if (device_state(&d) != Q4K_OK) return 0;
   if (is_decode(m)) {
-    q4k::DecodeQ8Plan p;
-    return q4k::decode_q8_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
+    q4k::DecodeQ8Plan p;  // one decode pass holds one h; calls of several passes have none to show
+    return m <= DECODE_CHUNK && q4k::decode_q8_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;
   }
   q4k::PrefillPlan p;
   return q4k::prefill_plan(m, hidden, inter, d->sms, &p) ? p.off_hq : 0;

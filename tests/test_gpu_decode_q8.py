@@ -158,14 +158,33 @@ def test_decode_q8_repeated_calls_on_the_same_buffers():
     assert np.array_equal(y.cpu().numpy().view(np.uint32), outs[0].view(np.uint32))
 
 
+@pytest.mark.parametrize("m", [9, 20, 32])
+def test_decode_q8_passes_of_8_tokens(m):
+    """9-32 tokens run as decode passes of at most 8 tokens: each pass's rows equal the call on
+    those tokens alone, and the whole output meets the Q8_1 oracle."""
+    c = workloads.small_config(1024, 1536, m, "f32", ("channels", 0.01, 50.0))
+    wg, wu, wd = workloads.weights(c)
+    dg, du, dd = to_dev(wg), to_dev(wu), to_dev(wd)
+    x, _ = workloads.activations(c)
+    ws = torch.empty(lib().ffn_q4k_q8_1_workspace_bytes(m, 1024, 1536), dtype=torch.uint8, device=dev())
+    y = lib().ffn_q4k_swiglu_q8_1(to_dev(x), dg, du, dd, ws).cpu().numpy()
+    for t0 in range(0, m, 8):
+        xs = x[t0:t0 + 8]
+        w1 = torch.empty(lib().ffn_q4k_q8_1_workspace_bytes(len(xs), 1024, 1536), dtype=torch.uint8, device=dev())
+        ys = lib().ffn_q4k_swiglu_q8_1(to_dev(xs), dg, du, dd, w1).cpu().numpy()
+        assert np.array_equal(y[t0:t0 + 8].view(np.uint32), ys.view(np.uint32))
+    assert rel_l2(y, oracle.ffn_prefill(x, wg, wu, wd)["y"]) <= ACCEPT
+    assert lib().ffn_q4k_q8_1_workspace_h_offset(m, 1024, 1536) == 0
+
+
 def test_q8_1_entry_point_at_prefill_sizes_is_the_prefill_path():
-    """For m >= 9 the Q8_1 entry point and ffn_q4k_swiglu_ex compute the same bytes."""
-    c = workloads.small_config(512, 768, 24, "bf16", ("channels", 0.01, 100.0))
+    """For m >= 33 the Q8_1 entry point and ffn_q4k_swiglu_ex compute the same bytes."""
+    c = workloads.small_config(512, 768, 48, "bf16", ("channels", 0.01, 100.0))
     wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
     _, xb = workloads.activations(c)
     xd = to_dev(xb)
-    ws1 = torch.zeros(lib().ffn_q4k_q8_1_workspace_bytes(24, 512, 768), dtype=torch.uint8, device=dev())
-    ws2 = torch.zeros(lib().ffn_q4k_workspace_bytes(24, 512, 768), dtype=torch.uint8, device=dev())
+    ws1 = torch.zeros(lib().ffn_q4k_q8_1_workspace_bytes(48, 512, 768), dtype=torch.uint8, device=dev())
+    ws2 = torch.zeros(lib().ffn_q4k_workspace_bytes(48, 512, 768), dtype=torch.uint8, device=dev())
     y1 = lib().ffn_q4k_swiglu_q8_1(xd, wg, wu, wd, ws1).cpu().numpy()
     y2 = lib().ffn_q4k_swiglu_ex(xd, wg, wu, wd, ws2).cpu().numpy()
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))

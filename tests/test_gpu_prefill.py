@@ -1,4 +1,4 @@
-"""Parity of the prefill path (m >= 9: Q8_1 activations, tcgen05 Q4_K x Q8_1 GEMM) with the oracle."""
+"""Parity of the prefill path (m >= 33: Q8_1 activations, tcgen05 Q4_K x Q8_1 GEMM) with the oracle."""
 import numpy as np
 import pytest
 
@@ -55,7 +55,7 @@ def _check(y, ref, hq_gpu, wd):
     return err
 
 
-@pytest.mark.parametrize("H,I,m", [(256, 256, 9), (256, 512, 16), (512, 256, 127), (256, 768, 128),
+@pytest.mark.parametrize("H,I,m", [(256, 256, 33), (256, 512, 48), (512, 256, 127), (256, 768, 128),
                                    (768, 512, 129), (1024, 1280, 200), (512, 2048, 257), (1280, 256, 64)])
 def test_prefill_shape_sweep(H, I, m):
     c = workloads.small_config(H, I, m, "bf16", ("channels", 0.01, 100.0))
@@ -84,10 +84,10 @@ def test_prefill_config4_sampled_tokens():
 
 
 def test_prefill_zero_input():
-    c = workloads.small_config(256, 512, 20, "bf16")
+    c = workloads.small_config(256, 512, 40, "bf16")
     wg, wu, wd = workloads.weights(c)
-    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(20, 256, 512), dtype=torch.uint8, device=dev())
-    x = torch.zeros((20, 256), dtype=torch.bfloat16, device=dev())
+    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(40, 256, 512), dtype=torch.uint8, device=dev())
+    x = torch.zeros((40, 256), dtype=torch.bfloat16, device=dev())
     y = lib().ffn_q4k_swiglu_ex(x, to_dev(wg), to_dev(wu), to_dev(wd), ws)
     assert torch.count_nonzero(y).item() == 0
 
