@@ -19,7 +19,7 @@ cudaError_t launch_q8_1(const void* x, int bf16, int64_t m, int64_t k, void* out
 cudaError_t launch_quantize_weights(const void* w, int bf16, int64_t rows, int64_t cols, void* out,
                                     uint32_t* err, cudaStream_t s);
 
-// ---------------------------------------------------------------- decode (m <= 8)
+// ---------------------------------------------------------------- decode (m <= 8 per pass)
 struct DecodePlan {
   int m, hidden, inter;
   int nt;              // n-tiles of 4 tokens (1 or 2)
@@ -34,7 +34,7 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
                           float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
 
-// ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8)
+// ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8 per pass)
 struct DecodeQ8Plan {
   int m, hidden, inter;
   int mt;              // tokens the GEMV kernels are compiled for (1, 2, 4 or 8; >= m)
@@ -65,7 +65,7 @@ cudaError_t launch_q6k_gemv(const Q6Plan& p, const void* x, int bf16, const void
                             uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
 cudaError_t launch_q6k_dequant(const void* w, float* out, int64_t rows, int64_t cols, cudaStream_t s);
 
-// ---------------------------------------------------------------- prefill (m >= 9)
+// ---------------------------------------------------------------- prefill (m >= 33)
 struct PrefillPlan {
   int m, hidden, inter;
   size_t ws_bytes;

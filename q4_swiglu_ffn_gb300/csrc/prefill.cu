@@ -1,4 +1,4 @@
-// Prefill regime (m >= 9 tokens) of the Q4_K SwiGLU FFN on sm_103a.
+// Prefill regime (m >= 33 tokens) of the Q4_K SwiGLU FFN on sm_103a.
 //
 //   P0 q8_1(x)             x -> planar Q8_1 (bit-exact; also the ABI's q8_1_quantize_act)
 //   P1 expand(xq)          Q8_1 -> tensor-core B operand planes (below)
