@@ -37,11 +37,11 @@
  *     rows of hidden/256 blocks, W_down holds `hidden` rows of inter/256
  *     blocks (row = output feature, blocks run along the input dimension;
  *     realizar q4k_gemv_cached_uses.rs, q4k_gemv_cached: n = output, k = input).
- *   - Regimes: m <= 32 runs the decode path (float32 activations, no
- *     activation quantization) in passes of at most 8 tokens; m >= 33 runs the
+ *   - Regimes: m <= 24 runs the decode path (float32 activations, no
+ *     activation quantization) in passes of at most 8 tokens; m >= 25 runs the
  *     prefill path (activations quantized to Q8_1, Q4_K x Q8_1 GEMM on the
  *     tensor cores). ffn_q4k_swiglu_q8_1 quantizes the activations to Q8_1 at
- *     every m (decode passes up to 32 tokens, the prefill path above).
+ *     every m (decode passes up to 24 tokens, the prefill path above).
  */
 #ifndef Q4KFFN_H
 #define Q4KFFN_H
@@ -134,9 +134,9 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
  * with exact integer inner sums. Source: realizar src/cuda/executor/layers/
  * ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (the decode pipeline with quantized
  * activations and integer dot products); spark_model/layers/ops/q4k_mmq.rs,
- * q4k_mmq_gemm (the block correction). For m = 1..32 it runs integer-dot GEMVs
+ * q4k_mmq_gemm (the block correction). For m = 1..24 it runs integer-dot GEMVs
  * in passes of at most 8 tokens (x Q8_1, gate+up GEMV, chunk sum + SwiGLU + Q8_1
- * of h, down GEMV, down chunk sum); for m >= 33 it is the same computation as
+ * of h, down GEMV, down chunk sum); for m >= 25 it is the same computation as
  * ffn_q4k_swiglu_ex's prefill path (and gives the same bytes). x is float32 or bf16 [m][hidden] (bf16 is
  * widened exactly before quantization), y float32 [m][hidden]. The workspace is
  * caller-owned, 256-byte aligned, of at least ffn_q4k_q8_1_workspace_bytes(m,
@@ -151,7 +151,7 @@ q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_
 size_t ffn_q4k_q8_1_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
 /* Test hook: byte offset, inside an ffn_q4k_swiglu_q8_1 workspace, of the
  * planar Q8_1 copy of h = silu(gate)*up (q8_1_bytes(m, inter) bytes) that the
- * call feeds to the down projection; 0 for an invalid shape and for 9..32
+ * call feeds to the down projection; 0 for an invalid shape and for 9..24
  * tokens (several decode passes, each with its own h). */
 size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter);
 /* Decode-regime variant of ffn_q4k_swiglu (float32 x, m = 1..8, hidden and
@@ -209,7 +209,7 @@ size_t ffn_q4k_workspace_bytes(int64_t m, int64_t hidden, int64_t inter);
 
 /* Byte offset and size, inside an ffn_q4k_swiglu_ex workspace, of the planar
  * Q8_1 copy of the activated vector h = silu(gate)*up that the prefill path
- * feeds to the down projection (m >= 33 only; test hook, offset 0 / size 0 for
+ * feeds to the down projection (m >= 25 only; test hook, offset 0 / size 0 for
  * decode shapes). */
 size_t ffn_q4k_workspace_h_q8_1_offset(int64_t m, int64_t hidden, int64_t inter);
 

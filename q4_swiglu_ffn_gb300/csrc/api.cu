@@ -79,12 +79,12 @@ q4k_status check_ffn_args(const void* x, int dtype, int64_t m, int64_t hidden, i
 }
 
 // Up to DECODE_MAX tokens the call runs the decode kernels, in passes of at most
-// DECODE_CHUNK tokens (their token tiles hold 8): one GEMV pass streams all the
-// weights in about the time of a full-tile prefill GEMM's first wave, so passes
-// win while there are at most four of them (m <= 32 on the workloads measured).
-// From 33 tokens on the prefill GEMM runs.
+// DECODE_CHUNK tokens (their token tiles hold 8). A pass streams all the weights
+// once; the prefill GEMM at one token tile costs about three passes, so passes
+// win up to 24 tokens on the workloads measured. From 25 tokens on the prefill
+// GEMM runs.
 constexpr int64_t DECODE_CHUNK = 8;
-constexpr int64_t DECODE_MAX = 32;
+constexpr int64_t DECODE_MAX = 24;
 bool is_decode(int64_t m) { return m <= DECODE_MAX; }
 int64_t last_chunk(int64_t m) { return m - DECODE_CHUNK * ((m - 1) / DECODE_CHUNK); }
 

@@ -65,13 +65,15 @@ cudaError_t launch_q6k_gemv(const Q6Plan& p, const void* x, int bf16, const void
                             uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
 cudaError_t launch_q6k_dequant(const void* w, float* out, int64_t rows, int64_t cols, cudaStream_t s);
 
-// ---------------------------------------------------------------- prefill (m >= 33)
+// ---------------------------------------------------------------- prefill (m >= 25)
 struct PrefillPlan {
   int m, hidden, inter;
   size_t ws_bytes;
   size_t off_xq, off_hq;  // planar Q8_1 of x and of h
   size_t off_xop, off_hop;  // tensor-core operands
   size_t off_misc;
+  int ksplit;             // K slices of the down projection
+  size_t off_ypart;       // their partial outputs [ksplit][m][hidden] (ksplit > 1)
 };
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,

@@ -1,4 +1,4 @@
-// Prefill regime (m >= 33 tokens) of the Q4_K SwiGLU FFN on sm_103a.
+// Prefill regime (m >= 25 tokens) of the Q4_K SwiGLU FFN on sm_103a.
 //
 //   P0 q8_1(x)             x -> planar Q8_1 (bit-exact; also the ABI's q8_1_quantize_act)
 //   P1 expand(xq)          Q8_1 -> tensor-core B operand planes (below)
@@ -34,14 +34,13 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemv_stream.cuh"
 #include "kernels.h"
 #include "tmap.h"
 
 namespace q4k {
 
 namespace {
-
-inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // ------------------------------------------------------------------------- expand
 // One CTA (256 threads) per token row. Writes
@@ -139,10 +138,11 @@ struct MmqParams {
   int m;               // tokens
   int ldo;             // output row length (inter for hq, hidden for y)
   int ntn;             // tiles along N (tokens)
+  int ksplit;          // slices of K: CTA b takes slice b / (gridDim / ksplit) (down only; 1 for gate/up)
   const float* tscale; // 2^e_t per token
   int8_t* hq_qs;       // gate/up: Q8_1 quants of h [m][inter]
   float2* hq_ds;       // gate/up: Q8_1 (d, s) of h [m][inter/32]
-  float* y;            // down: [m][hidden]
+  float* y;            // down: [ksplit][m][hidden] (the slices' partial sums, or y itself when ksplit = 1)
   uint32_t* err;
 };
 
@@ -262,7 +262,9 @@ __device__ __forceinline__ void gateup_final(const uint8_t* smem, const MmqParam
   }
 }
 
-template <bool GATEUP>
+// SPLIT: the CTAs of each (row tile, token tile) split K into P.ksplit slices
+// (the down projection at small m); without it every CTA takes all of K.
+template <bool GATEUP, bool SPLIT>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     mmq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constant__ CUtensorMap tm_lo,
                const __grid_constant__ CUtensorMap tm_mn, const MmqParams P) {
@@ -276,7 +278,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x % P.ntn, mt = blockIdx.x / P.ntn;
+  const int tiles = SPLIT ? (int)gridDim.x / P.ksplit : (int)gridDim.x;  // (row tile, token tile) pairs
+  const int ks = SPLIT ? (int)blockIdx.x / tiles : 0, tile = (int)blockIdx.x - ks * tiles;
+  const int nt = tile % P.ntn, mt = tile / P.ntn;
+  // this CTA's superblocks [sb0, sb0 + nsbl); the loops below count from 0
+  const int sb0 = SPLIT ? (int)((int64_t)P.nsb * ks / P.ksplit) : 0;
+  const int nsbl = SPLIT ? (int)((int64_t)P.nsb * (ks + 1) / P.ksplit) - sb0 : P.nsb;
   const int64_t rowbytes = (int64_t)P.nsb * BLK;
 
   if (threadIdx.x == 0) {
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nchunks = P.nsb * CH_PER_SB;
+  const int nchunks = nsbl * CH_PER_SB;
 
   if (warp == W_TMA) {
     // ------------------------------------------------------------ TMA producer (B operand)
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         const int s = q % STAGES, u = q / STAGES;
         if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) break;
         uint8_t* st = smem + s * STAGE_BYTES;
-        const int sb = q / CH_PER_SB, c = q % CH_PER_SB;
+        const int sb = sb0 + q / CH_PER_SB, c = q % CH_PER_SB;
         if (c < 4) {
           mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
           tma_load_2d(st + TILE_BYTES, &tm_hi, sb * QK + c * KCH, nt * TN, &full[s]);
@@ -324,7 +331,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int sb = 0; sb < P.nsb && !*abort_flag; ++sb) {
+      for (int sb = 0; sb < nsbl && !*abort_flag; ++sb) {
         const int ab = sb & 1;
         if (sb >= 2 && !wait_bar(&acce[ab], ((sb - 2) >> 1) & 1, abort_flag, P.err)) break;
         tc_fence_after();
@@ -360,17 +367,18 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       src = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
     else
       src = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
+    src += (int64_t)sb0 * BLK;
     const uint32_t rsw = (uint32_t)(r & 7);
     uint8_t* arow_base = smem + (r >> 3) * 1024 + (r & 7) * 128;  // + stage offset
     uint4 raw[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
     bool ok = true;
-    for (int sb = 0; sb < P.nsb && ok; ++sb) {
+    for (int sb = 0; sb < nsbl && ok; ++sb) {
       uint4 cur[9];
 #pragma unroll
       for (int i = 0; i < 9; ++i) cur[i] = raw[i];
-      if (sb + 1 < P.nsb) {
+      if (sb + 1 < nsbl) {
 #pragma unroll
         for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(sb + 1) * BLK) + i);
       }
@@ -433,12 +441,13 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       hdr = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
     else
       hdr = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
+    hdr += (int64_t)sb0 * BLK;
     float acc[TN];
 #pragma unroll
     for (int i = 0; i < TN; ++i) acc[i] = 0.f;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     bool ok = true;
-    for (int sb = 0; sb < P.nsb; ++sb) {
+    for (int sb = 0; sb < nsbl; ++sb) {
       const int ab = sb & 1;
       const uint32_t dm2 = __ldg(reinterpret_cast<const uint32_t*>(hdr + (int64_t)sb * BLK));
       const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
@@ -478,10 +487,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       gateup_final(smem, P, mt, nt, 4 + (warp - W_EPI), lane, abort_flag);
     } else if (ok) {
       const int row = mt * TM + r;
+      float* yo = P.y + (int64_t)ks * P.m * P.ldo;
 #pragma unroll
       for (int i = 0; i < TN; ++i) {
         const int t = t0 + i;
-        if (t < P.m) P.y[(int64_t)t * P.ldo + row] = acc[i] * P.tscale[t];
+        if (t < P.m) yo[(int64_t)t * P.ldo + row] = acc[i] * P.tscale[t];
       }
     }
   }
@@ -508,10 +518,10 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
                  TN, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <bool GATEUP>
+template <bool GATEUP, bool SPLIT>
 cudaError_t launch_mmq(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& mn, const MmqParams& P,
                        int grid, cudaStream_t s) {
-  auto kern = mmq_kernel<GATEUP>;
+  auto kern = mmq_kernel<GATEUP, SPLIT>;
   static uint64_t attr_set = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -532,9 +542,21 @@ struct Operand {
 
 }  // namespace
 
+// K slices of the down projection: its (row tile, token tile) CTAs number only
+// hidden/128 per 128 tokens, fewer than the SMs when m is small. Each slice sums
+// part of K into its own partial output, reduced in slice order afterwards. The
+// grid is split as far as all slices still run in one wave (and each keeps at
+// least two superblocks); a grid of a wave or more is not split, since the
+// partial outputs cost traffic that a full grid does not repay.
+int down_ksplit(int64_t m, int64_t hidden, int64_t inter, int num_sms) {
+  const int64_t ctas = (hidden / TM) * ((m + TN - 1) / TN), nsb = inter / QK;
+  int k = 1;
+  while (k < 8 && ctas * (k + 1) <= num_sms && nsb / (k + 1) >= 2) ++k;
+  return k;
+}
+
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p) {
-  (void)num_sms;
-  if (m < 9) return false;
+  if (m < 9 || num_sms < 1) return false;
   p->m = (int)m;
   p->hidden = (int)hidden;
   p->inter = (int)inter;
@@ -553,6 +575,8 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   p->off_xop = take(op_bytes(hidden, true));
   p->off_hop = take(op_bytes(inter, true));
   p->off_misc = take(256);
+  p->ksplit = down_ksplit(m, hidden, inter, num_sms);
+  p->off_ypart = take(p->ksplit > 1 ? (size_t)p->ksplit * m * hidden * 4 : 0);
   p->ws_bytes = o;
   return true;
 }
@@ -604,12 +628,13 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.m = (int)m;
   g.ldo = (int)I;
   g.ntn = ntn;
+  g.ksplit = 1;
   g.tscale = xo.scale;
   g.hq_qs = hq;
   g.hq_ds = hds;
   g.err = err;
   prof.before(2, s);
-  e = launch_mmq<true>(mx_hi, mx_lo, mx_mn, g, (int)(I / 64) * ntn, s);
+  e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, (int)(I / 64) * ntn, s);
   prof.after(2, s);
   if (e != cudaSuccess) return e;
 
@@ -624,11 +649,15 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.m = (int)m;
   dn.ldo = (int)H;
   dn.ntn = ntn;
+  dn.ksplit = p.ksplit;
   dn.tscale = ho.scale;
-  dn.y = y;
+  float* ypart = (float*)(W + p.off_ypart);
+  dn.y = p.ksplit > 1 ? ypart : y;
   dn.err = err;
-  prof.before(4, s);
-  e = launch_mmq<false>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn, s);
+  prof.before(4, s);  // the down MMQ, and the sum of its K slices when there are several
+  e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn * p.ksplit, s)
+                   : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn, s);
+  if (e == cudaSuccess && p.ksplit > 1) e = launch_finish_down(ypart, p.ksplit, m * H, y, s);
   prof.after(4, s);
   return e;
 }

@@ -117,9 +117,9 @@ def test_workspace_too_small_is_rejected():
     assert e.value.status == 8
 
 
-@pytest.mark.parametrize("m", [9, 16, 17, 31, 32])
+@pytest.mark.parametrize("m", [9, 16, 17, 23, 24])
 def test_decode_passes_of_8_tokens(m):
-    """9-32 tokens run as decode passes of at most 8 tokens (float32 activations): each pass's
+    """9-24 tokens run as decode passes of at most 8 tokens (float32 activations): each pass's
     rows equal the call on those tokens alone, and the whole output meets the fp64 oracle."""
     c = workloads.small_config(1024, 1536, m, "f32", ("channels", 0.01, 50.0))
     wg, wu, wd = workloads.weights(c)

@@ -158,9 +158,9 @@ def test_decode_q8_repeated_calls_on_the_same_buffers():
     assert np.array_equal(y.cpu().numpy().view(np.uint32), outs[0].view(np.uint32))
 
 
-@pytest.mark.parametrize("m", [9, 20, 32])
+@pytest.mark.parametrize("m", [9, 20, 24])
 def test_decode_q8_passes_of_8_tokens(m):
-    """9-32 tokens run as decode passes of at most 8 tokens: each pass's rows equal the call on
+    """9-24 tokens run as decode passes of at most 8 tokens: each pass's rows equal the call on
     those tokens alone, and the whole output meets the Q8_1 oracle."""
     c = workloads.small_config(1024, 1536, m, "f32", ("channels", 0.01, 50.0))
     wg, wu, wd = workloads.weights(c)
@@ -178,7 +178,7 @@ def test_decode_q8_passes_of_8_tokens(m):
 
 
 def test_q8_1_entry_point_at_prefill_sizes_is_the_prefill_path():
-    """For m >= 33 the Q8_1 entry point and ffn_q4k_swiglu_ex compute the same bytes."""
+    """For m >= 25 the Q8_1 entry point and ffn_q4k_swiglu_ex compute the same bytes."""
     c = workloads.small_config(512, 768, 48, "bf16", ("channels", 0.01, 100.0))
     wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
     _, xb = workloads.activations(c)
