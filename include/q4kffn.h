@@ -126,6 +126,15 @@ q4k_status ffn_q4k_swiglu_ex(const void* x, q4k_dtype dtype, int64_t m, int64_t 
                              const void* W_down, float* y, void* workspace, size_t ws_bytes,
                              q4k_stream_t stream);
 
+/* As ffn_q4k_swiglu_ex, with the dtype of y: Q4K_F32, or Q4K_BF16 (each output
+ * is the float32 result rounded once to bf16, round to nearest even, by the
+ * final kernel that sums the down projection's K-chunks). Source: spark_model/
+ * layers/ops/q4k_mmq.rs, q4k_mmq_gemm (the MMQ's fused bf16 store). y is
+ * [m][hidden] of that dtype; the workspace is sized by ffn_q4k_workspace_bytes. */
+q4k_status ffn_q4k_swiglu_ex_y(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden,
+                               int64_t inter, const void* W_gate, const void* W_up,
+                               const void* W_down, void* y, q4k_dtype ydtype, void* workspace,
+                               size_t ws_bytes, q4k_stream_t stream);
 /* The feed-forward block with Q8_1 activations at every m: x is quantized to
  * Q8_1 once and shared by the gate and up projections, h = silu(g) * u is
  * re-quantized to Q8_1 before the down projection, and every dot product is

@@ -34,6 +34,7 @@ _SIGS = {
     "ffn_q4k_swiglu": (_int, [_p, _i64, _i64, _i64, _p, _p, _p, _p, _p]),
     "ffn_q4k_swiglu_ex": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
     "ffn_q4k_swiglu_q8_1": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _p, _sz, _p]),
+    "ffn_q4k_swiglu_ex_y": (_int, [_p, _int, _i64, _i64, _i64, _p, _p, _p, _p, _int, _p, _sz, _p]),
     "ffn_q4k_q8_1_workspace_bytes": (_sz, [_i64, _i64, _i64]),
     "ffn_q4k_q8_1_workspace_h_offset": (_sz, [_i64, _i64, _i64]),
     "ffn_q4k_workspace_bytes": (_sz, [_i64, _i64, _i64]),
@@ -153,6 +154,16 @@ def ffn_q4k_swiglu_ex(x, W_gate, W_up, W_down, workspace, y=None, stream=None):
     _check(lib.ffn_q4k_swiglu_ex(_ptr(x), _dtype_code(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up),
                                  _ptr(W_down), _ptr(y), _ptr(workspace), workspace.numel(), _stream(stream)),
            "ffn_q4k_swiglu_ex")
+    return y
+
+
+def ffn_q4k_swiglu_ex_y(x, W_gate, W_up, W_down, workspace, y):
+    """As ffn_q4k_swiglu_ex, writing y as float32 or bf16 (the dtype of the given y tensor)."""
+    m, hidden = x.shape
+    inter = W_gate.shape[0]
+    _check(lib.ffn_q4k_swiglu_ex_y(_ptr(x), _dtype_code(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up),
+                                   _ptr(W_down), _ptr(y), _dtype_code(y), _ptr(workspace), workspace.numel(),
+                                   _stream(None)), "ffn_q4k_swiglu_ex_y")
     return y
 
 

@@ -155,6 +155,7 @@ struct DecodeGraph {
   const void *x = nullptr, *wg = nullptr, *wu = nullptr, *wd = nullptr, *ws = nullptr;
   float* y = nullptr;
   int dtype = 0;
+  int ybf16 = 0;  // y stored as bf16
   int64_t m = 0, hidden = 0, inter = 0;
   uint64_t last = 0;
   cudaGraphExec_t exec = nullptr;
@@ -181,8 +182,8 @@ q4k_status run_graphed(const DecodeGraph& key, cudaStream_t s, Launch launch) {
   ++gc.tick;
   for (DecodeGraph& g : gc.g)
     if (g.used && g.path == key.path && g.x == key.x && g.y == key.y && g.wg == key.wg && g.wu == key.wu &&
-        g.wd == key.wd && g.ws == key.ws && g.dtype == key.dtype && g.m == key.m && g.hidden == key.hidden &&
-        g.inter == key.inter) {
+        g.wd == key.wd && g.ws == key.ws && g.dtype == key.dtype && g.ybf16 == key.ybf16 && g.m == key.m &&
+        g.hidden == key.hidden && g.inter == key.inter) {
       g.last = gc.tick;
       return cudaGraphLaunch(g.exec, s) == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
     }
@@ -220,13 +221,13 @@ q4k_status run_graphed(const DecodeGraph& key, cudaStream_t s, Launch launch) {
 }
 
 q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
-                      const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+                      const void* wd, void* y, int ybf16, void* ws, DeviceState* d, cudaStream_t s) {
   DecodeGraph key;
   key.path = 0;
-  key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = y;
-  key.dtype = dtype, key.m = p.m, key.hidden = p.hidden, key.inter = p.inter;
+  key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = static_cast<float*>(y);
+  key.dtype = dtype, key.ybf16 = ybf16, key.m = p.m, key.hidden = p.hidden, key.inter = p.inter;
   return run_graphed(key, s, [&](cudaStream_t st, const q4k::ProfileEvents& pr) {
-    return q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, st, pr);
+    return q4k::launch_decode(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, st, pr, ybf16);
   });
 }
 
@@ -253,7 +254,9 @@ q4k_status run_q6k(const q4k::Q6Plan& p, const void* x, int dtype, const void* w
 }
 
 q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t inter, const void* wg,
-                   const void* wu, const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+                   const void* wu, const void* wd, void* y, void* ws, DeviceState* d, cudaStream_t s,
+                   int ybf16 = 0) {
+  const int64_t yrow = hidden * (ybf16 ? 2 : 4);  // bytes of one token of y
   cudaError_t e;
   if (is_decode(m)) {
     const int64_t xrow = hidden * (dtype == Q4K_BF16 ? 2 : 4);  // bytes of one token of x
@@ -261,14 +264,14 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
       q4k::DecodePlan p;
       if (!q4k::decode_plan(std::min(DECODE_CHUNK, m - t0), hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
       const q4k_status st = run_decode(p, static_cast<const uint8_t*>(x) + t0 * xrow, dtype, wg, wu, wd,
-                                       y + t0 * hidden, ws, d, s);
+                                       static_cast<uint8_t*>(y) + t0 * yrow, ybf16, ws, d, s);
       if (st != Q4K_OK) return st;
     }
     return Q4K_OK;
   } else {
     q4k::PrefillPlan p;
     if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
-    e = q4k::launch_prefill(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof);
+    e = q4k::launch_prefill(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof, ybf16);
   }
   return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -387,6 +390,29 @@ q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_
     if (st != Q4K_OK) return fail(st);
   }
   return Q4K_OK;
+}
+
+q4k_status ffn_q4k_swiglu_ex_y(const void* x, q4k_dtype dtype, int64_t m, int64_t hidden, int64_t inter,
+                               const void* W_gate, const void* W_up, const void* W_down, void* y, q4k_dtype ydtype,
+                               void* workspace, size_t ws_bytes, q4k_stream_t stream) {
+  if (ydtype != Q4K_F32 && ydtype != Q4K_BF16) return fail(Q4K_ERR_DTYPE);
+  q4k_status st = check_ffn_args(x, dtype, m, hidden, inter, W_gate, W_up, W_down, static_cast<const float*>(y));
+  if (st != Q4K_OK) return fail(st);
+  if (!workspace) return fail(Q4K_ERR_NULL);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4K_ERR_ALIGN);
+  DeviceState* d = nullptr;
+  st = device_state(&d);
+  if (st != Q4K_OK) return fail(st);
+  const void* yy = y;
+  st = resolve_io(x, &x);
+  if (st == Q4K_OK) st = resolve_io(y, &yy);
+  if (st != Q4K_OK) return fail(st);
+  const size_t need = plan_bytes(m, hidden, inter, d->sms);
+  if (need == 0) return fail(Q4K_ERR_SHAPE);
+  if (ws_bytes < need) return fail(Q4K_ERR_NOMEM);
+  st = run_ffn(x, dtype, m, hidden, inter, W_gate, W_up, W_down, const_cast<void*>(yy), workspace, d,
+               (cudaStream_t)stream, ydtype == Q4K_BF16);
+  return st == Q4K_OK ? st : fail(st);
 }
 
 size_t ffn_q4k_q8_1_workspace_bytes(int64_t m, int64_t hidden, int64_t inter) {

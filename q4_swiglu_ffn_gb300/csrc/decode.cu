@@ -562,18 +562,19 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   p->off_fm2 = take((size_t)nsb2 * p->nt * 32 * 4);
   p->off_sc2 = take((size_t)nsb2 * 8 * 4);
   p->off_p1 = take((size_t)p->nks1 * 2 * m * inter * 4);
-  p->off_p2 = take(p->nks2 > 1 ? (size_t)p->nks2 * m * hidden * 4 : 0);
+  p->off_p2 = take((size_t)p->nks2 * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
 }
 
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
-                          float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof) {
+                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16) {
   uint8_t* W = (uint8_t*)ws;
   FragPtrs f1{(uint2*)(W + p.off_fx1), (uint32_t*)(W + p.off_fm1), (float*)(W + p.off_sc1)};
   FragPtrs f2{(uint2*)(W + p.off_fx2), (uint32_t*)(W + p.off_fm2), (float*)(W + p.off_sc2)};
   float* p1 = (float*)(W + p.off_p1);
-  float* p2 = p.nks2 > 1 ? (float*)(W + p.off_p2) : y;
+  const bool k3 = p.nks2 > 1 || ybf16;  // K3 sums the chunks and/or stores bf16
+  float* p2 = k3 ? (float*)(W + p.off_p2) : (float*)y;
   const int nsb1 = p.hidden / QK, nsb2 = p.inter / QK;
   const bool one = p.nt == 1;
   const int sl1 = one ? Shape<true, 1>::SLICES : Shape<true, 2>::SLICES;
@@ -618,7 +619,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   if (e != cudaSuccess) return e;
 
   prof.before(4, s);  // the down-chunk sum (absent when K is not split)
-  if (p.nks2 > 1) e = launch_finish_down(p2, p.nks2, (int64_t)p.m * p.hidden, y, s);
+  if (k3) e = launch_finish_down(p2, p.nks2, (int64_t)p.m * p.hidden, y, ybf16, s);
   prof.after(4, s);
   return e;
 }

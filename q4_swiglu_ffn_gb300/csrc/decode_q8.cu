@@ -575,21 +575,22 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
   p->off_xq = take((size_t)m * hidden + (size_t)m * (hidden / Q8B) * 8);
   p->off_hq = take((size_t)m * inter + (size_t)m * (inter / Q8B) * 8);
   p->off_p1 = take((size_t)p->nks1 * 2 * m * inter * 4);
-  p->off_p2 = take(p->nks2 > 1 ? (size_t)p->nks2 * m * hidden * 4 : 0);
+  p->off_p2 = take((size_t)p->nks2 * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
 }
 
 cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, const void* wg, const void* wu,
-                             const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
-                             const ProfileEvents& prof) {
+                             const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
+                             const ProfileEvents& prof, int ybf16) {
   uint8_t* W = (uint8_t*)ws;
   uint8_t* xq = W + p.off_xq;
   uint8_t* hq = W + p.off_hq;
   const float4* xds = (const float4*)(xq + (size_t)p.m * p.hidden);
   float2* hds = (float2*)(hq + (size_t)p.m * p.inter);
   float* p1 = (float*)(W + p.off_p1);
-  float* p2 = p.nks2 > 1 ? (float*)(W + p.off_p2) : y;
+  const bool k3 = p.nks2 > 1 || ybf16;  // K3 sums the chunks and/or stores bf16
+  float* p2 = k3 ? (float*)(W + p.off_p2) : (float*)y;
   const int nsb1 = p.hidden / QK, nsb2 = p.inter / QK;
   int cb1, sl1, cps1, cb2, sl2, cps2;
   shape_q8<true>(p.mt, &cb1, &sl1, &cps1);
@@ -631,7 +632,7 @@ cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, con
   if (e != cudaSuccess) return e;
 
   prof.before(4, s);  // the down-chunk sum (absent when K is not split)
-  if (p.nks2 > 1) e = launch_finish_down(p2, p.nks2, (int64_t)p.m * p.hidden, y, s);
+  if (k3) e = launch_finish_down(p2, p.nks2, (int64_t)p.m * p.hidden, y, ybf16, s);
   prof.after(4, s);
   return e;
 }

@@ -22,8 +22,20 @@ __device__ __forceinline__ void tma_box3(void* dst, const CUtensorMap* tm, int r
       : "memory");
 }
 
-// y = sum over the K-chunks of the down partials, in chunk order.
-__global__ void finish_down_kernel(const float* __restrict__ part, int nks, int64_t n, float* __restrict__ y) {
+__device__ __forceinline__ void store4(float* y, int64_t i, float4 s) { reinterpret_cast<float4*>(y)[i] = s; }
+__device__ __forceinline__ void store4(__nv_bfloat16* y, int64_t i, float4 s) {
+  // round to nearest even, once
+  const __nv_bfloat162 a = __floats2bfloat162_rn(s.x, s.y), b = __floats2bfloat162_rn(s.z, s.w);
+  uint2 v;
+  v.x = *reinterpret_cast<const uint32_t*>(&a);
+  v.y = *reinterpret_cast<const uint32_t*>(&b);
+  reinterpret_cast<uint2*>(y)[i] = v;
+}
+
+// y = sum over the K-chunks of the down partials, in chunk order (float32, or
+// bf16 rounded once from the float32 sum).
+template <typename T>
+__global__ void finish_down_kernel(const float* __restrict__ part, int nks, int64_t n, T* __restrict__ y) {
   pdl_launch_dependents();
   pdl_wait();
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -34,7 +46,7 @@ __global__ void finish_down_kernel(const float* __restrict__ part, int nks, int6
     const float4 a = reinterpret_cast<const float4*>(part + (int64_t)k * n)[i];
     s.x += a.x, s.y += a.y, s.z += a.z, s.w += a.w;
   }
-  reinterpret_cast<float4*>(y)[i] = s;
+  store4(y, i, s);
 }
 
 inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
@@ -51,12 +63,14 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// Launches K3 (n = m * hidden outputs) when the down projection was split along K.
-inline cudaError_t launch_finish_down(const float* part, int nks, int64_t n, float* y, cudaStream_t s) {
+// Launches K3 (n = m * hidden outputs): the sum of the down projection's K-chunks,
+// and the store of y as float32 or (ybf16) bf16.
+inline cudaError_t launch_finish_down(const float* part, int nks, int64_t n, void* y, int ybf16, cudaStream_t s) {
   void* args[] = {&part, &nks, &n, &y};
+  const void* fn = ybf16 ? reinterpret_cast<const void*>(finish_down_kernel<__nv_bfloat16>)
+                         : reinterpret_cast<const void*>(finish_down_kernel<float>);
   // small CTAs spread the sums over more SMs (more loads in flight)
-  return launch_pdl(reinterpret_cast<const void*>(finish_down_kernel), dim3((unsigned)((n / 4 + 63) / 64)), dim3(64),
-                    0, s, args);
+  return launch_pdl(fn, dim3((unsigned)((n / 4 + 63) / 64)), dim3(64), 0, s, args);
 }
 
 // Weight matrix [rows][nsb blocks] as a 3-D tensor {18 x 8-byte elements of a

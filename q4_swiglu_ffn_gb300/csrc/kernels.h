@@ -31,8 +31,9 @@ struct DecodePlan {
   size_t off_fx1, off_fm1, off_sc1, off_fx2, off_fm2, off_sc2, off_p1, off_p2;
 };
 bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p);
+// y is float32, or bf16 when ybf16 (rounded once by the final chunk-sum kernel).
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
-                          float* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof);
+                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16 = 0);
 
 // ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8 per pass)
 struct DecodeQ8Plan {
@@ -48,8 +49,8 @@ struct DecodeQ8Plan {
 int decode_q8_tokens(int64_t m);
 bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodeQ8Plan* p);
 cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, const void* wg, const void* wu,
-                             const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
-                             const ProfileEvents& prof);
+                             const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
+                             const ProfileEvents& prof, int ybf16 = 0);
 
 // ---------------------------------------------------------------- Q6_K GEMV (m <= 8)
 struct Q6Plan {
@@ -77,7 +78,7 @@ struct PrefillPlan {
 };
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
-                           const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
-                           const ProfileEvents& prof);
+                           const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
+                           const ProfileEvents& prof, int ybf16 = 0);
 
 }  // namespace q4k

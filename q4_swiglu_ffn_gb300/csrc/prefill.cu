@@ -576,14 +576,14 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   p->off_hop = take(op_bytes(inter, true));
   p->off_misc = take(256);
   p->ksplit = down_ksplit(m, hidden, inter, num_sms);
-  p->off_ypart = take(p->ksplit > 1 ? (size_t)p->ksplit * m * hidden * 4 : 0);
+  p->off_ypart = take((size_t)p->ksplit * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
 }
 
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
-                           const void* wd, float* y, void* ws, uint32_t* err, cudaStream_t s,
-                           const ProfileEvents& prof) {
+                           const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
+                           const ProfileEvents& prof, int ybf16) {
   uint8_t* W = (uint8_t*)ws;
   const int64_t m = p.m, H = p.hidden, I = p.inter;
   auto split = [&](uint8_t* base, int64_t k, bool with_lo) {
@@ -652,12 +652,13 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.ksplit = p.ksplit;
   dn.tscale = ho.scale;
   float* ypart = (float*)(W + p.off_ypart);
-  dn.y = p.ksplit > 1 ? ypart : y;
+  const bool fin = p.ksplit > 1 || ybf16;  // the slice sum and/or the bf16 store
+  dn.y = fin ? ypart : (float*)y;
   dn.err = err;
   prof.before(4, s);  // the down MMQ, and the sum of its K slices when there are several
   e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn * p.ksplit, s)
                    : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn, s);
-  if (e == cudaSuccess && p.ksplit > 1) e = launch_finish_down(ypart, p.ksplit, m * H, y, s);
+  if (e == cudaSuccess && fin) e = launch_finish_down(ypart, p.ksplit, m * H, y, ybf16, s);
   prof.after(4, s);
   return e;
 }
