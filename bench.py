@@ -291,7 +291,8 @@ def gpu_decode(args, rank, world, dist, path="f32"):
         torch.cuda.synchronize()
         e2e_copy_ms = f0.elapsed_time(f1)
     assert q.q4k_check_device_error() == 0
-    launches = 4 + (1 if kern_ms[4] > 1e-4 else 0)
+    step(0)
+    launches = q.q4k_last_call_kernels()
     return {"ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "e2e_copy_ms": e2e_copy_ms,
             "E": E, "R": R,
             "wbytes": wbytes, "xbytes": x_np.nbytes, "launches_per_step": launches, "pct": pct, "G": G}

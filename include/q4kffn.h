@@ -252,6 +252,9 @@ q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream);
  * whole call leave the hook off. */
 q4k_status q4k_set_profile_events(void* const* events, int n);
 
+/* Benchmark hook: how many kernels the most recent FFN or Q6_K GEMV call on
+ * this thread launched (directly, or as nodes of the replayed graph). */
+int q4k_last_call_kernels(void);
 /* Status of the most recent failed host-side call on this thread (Q4K_OK if none). */
 q4k_status q4k_get_last_error(void);
 

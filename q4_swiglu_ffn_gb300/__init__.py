@@ -48,6 +48,7 @@ _SIGS = {
     "q4k_test_bounded_wait": (_int, [ctypes.c_uint64, _p]),
     "q4k_set_profile_events": (_int, [_p, _int]),
     "q4k_get_last_error": (_int, []),
+    "q4k_last_call_kernels": (_int, []),
     "q4k_status_string": (ctypes.c_char_p, [_int]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -241,6 +242,11 @@ def q4k_set_profile_events(events) -> None:
 
 
 _prof_keep = None
+
+
+def q4k_last_call_kernels() -> int:
+    """Kernels the last FFN or Q6_K GEMV call on this thread launched (benchmark hook)."""
+    return lib.q4k_last_call_kernels()
 
 
 def q4k_get_last_error() -> int:

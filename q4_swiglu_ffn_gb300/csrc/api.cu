@@ -19,6 +19,7 @@ namespace {
 
 thread_local q4k_status g_last = Q4K_OK;
 thread_local q4k::ProfileEvents g_prof;
+thread_local int g_kernels = 0;  // kernels the last FFN or GEMV call launched (or replayed)
 
 q4k_status fail(q4k_status s) {
   g_last = s;
@@ -222,6 +223,7 @@ q4k_status run_graphed(const DecodeGraph& key, cudaStream_t s, Launch launch) {
 
 q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
                       const void* wd, void* y, int ybf16, void* ws, DeviceState* d, cudaStream_t s) {
+  g_kernels += 4 + (p.nks2 > 1 || ybf16);  // K0, K1, K1b, K2 (+ K3)
   DecodeGraph key;
   key.path = 0;
   key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = static_cast<float*>(y);
@@ -233,6 +235,7 @@ q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const 
 
 q4k_status run_decode_q8(const q4k::DecodeQ8Plan& p, const void* x, int dtype, const void* wg, const void* wu,
                          const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
+  g_kernels += 4 + (p.nks2 > 1);  // K0, K1, K1b, K2 (+ K3)
   DecodeGraph key;
   key.path = 1;
   key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = y;
@@ -244,6 +247,7 @@ q4k_status run_decode_q8(const q4k::DecodeQ8Plan& p, const void* x, int dtype, c
 
 q4k_status run_q6k(const q4k::Q6Plan& p, const void* x, int dtype, const void* w, float* y, void* ws, DeviceState* d,
                    cudaStream_t s) {
+  g_kernels = 2;
   DecodeGraph key;
   key.path = 2;
   key.x = x, key.wg = w, key.ws = ws, key.y = y;
@@ -260,6 +264,7 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
   cudaError_t e;
   if (is_decode(m)) {
     const int64_t xrow = hidden * (dtype == Q4K_BF16 ? 2 : 4);  // bytes of one token of x
+    g_kernels = 0;
     for (int64_t t0 = 0; t0 < m; t0 += DECODE_CHUNK) {
       q4k::DecodePlan p;
       if (!q4k::decode_plan(std::min(DECODE_CHUNK, m - t0), hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
@@ -271,6 +276,7 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
   } else {
     q4k::PrefillPlan p;
     if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
+    g_kernels = 5 + (p.ksplit > 1 || ybf16);  // Q8_1, expand, MMQ, expand, MMQ (+ slice sum)
     e = q4k::launch_prefill(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof, ybf16);
   }
   return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
@@ -382,6 +388,7 @@ q4k_status ffn_q4k_swiglu_q8_1(const void* x, q4k_dtype dtype, int64_t m, int64_
     return st == Q4K_OK ? st : fail(st);
   }
   const int64_t xrow = hidden * (dtype == Q4K_BF16 ? 2 : 4);  // bytes of one token of x
+  g_kernels = 0;
   for (int64_t t0 = 0; t0 < m; t0 += DECODE_CHUNK) {
     q4k::DecodeQ8Plan p;
     if (!q4k::decode_q8_plan(std::min(DECODE_CHUNK, m - t0), hidden, inter, d->sms, &p)) return fail(Q4K_ERR_SHAPE);
@@ -547,6 +554,8 @@ q4k_status q4k_set_profile_events(void* const* events, int n) {
 }
 
 q4k_status q4k_get_last_error(void) { return g_last; }
+
+int q4k_last_call_kernels(void) { return g_kernels; }
 
 const char* q4k_status_string(q4k_status s) {
   switch (s) {

@@ -493,15 +493,17 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes: 8 warps with two tiles per warp (gate and up of the same rows;
-// two adjacent W_down tiles) sharing the B operand. K1 loads gate and up boxes
-// of 16 rows x 8 superblocks, K2 one box of 64 rows x 4 superblocks (36.9 KB
-// per stage). Up to 4 tokens: two CTAs per SM (they drift apart, so one's loads
-// and waits overlap the other's arithmetic), two stages each. 5-8 tokens (two
-// token tiles, twice the registers for B): one CTA per SM, four stages.
+// CTA shapes: 8 warps. K1: two tiles per warp (gate and up of the same rows)
+// sharing the B operand, gate and up boxes of 16 rows x 8 superblocks. Up to 4
+// tokens: two CTAs per SM (they drift apart, so one's loads and waits overlap
+// the other's arithmetic); K1 two stages; K2 one 16-row tile per unit and warp
+// (boxes of 16 rows x 8 superblocks, three stages), which gives enough units to
+// leave K unsplit on large layers, so no chunk sum follows. 5-8 tokens (two
+// token tiles, twice the registers for B): one CTA per SM, four stages, K2 boxes
+// of 64 rows x 4 superblocks.
 template <bool GATEUP, int NT> struct Shape;
 template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
-template <> struct Shape<false, 1> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2; };
+template <> struct Shape<false, 1> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 8, STAGES = 3, CPS = 2; };
 template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 4, CPS = 1; };
 template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4, CPS = 1; };
 
@@ -546,7 +548,8 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   const int ctas1 = num_sms * (one ? Shape<true, 1>::CPS : Shape<true, 2>::CPS);
   const int ctas2 = num_sms * (one ? Shape<false, 1>::CPS : Shape<false, 2>::CPS);
   choose_split((nsb1 + sl1 - 1) / sl1, nru1, ctas1, max_nks, &p->nks1, &p->kc1);
-  choose_split((nsb2 + sl2 - 1) / sl2, nru2, ctas2, max_nks, &p->nks2, &p->kc2);
+  // K2 leaves K unsplit when its row units alone fill half the CTA slots (no chunk sum to follow)
+  choose_split((nsb2 + sl2 - 1) / sl2, nru2, ctas2, (one && 2 * nru2 >= ctas2) ? 1 : max_nks, &p->nks2, &p->kc2);
   p->grid1 = (int)std::min<int64_t>(ctas1, (int64_t)p->nks1 * nru1);
   p->grid2 = (int)std::min<int64_t>(ctas2, (int64_t)p->nks2 * nru2);
   size_t o = 0;
