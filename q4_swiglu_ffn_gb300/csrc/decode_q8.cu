@@ -447,15 +447,18 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes: 8 warps, each warp two tiles (K1: gate and up boxes of 16 rows x
-// 8 superblocks; K2: one box of 64 rows x 4 superblocks), two CTAs per SM, two
-// stages.
+// CTA shapes: 8 warps, two CTAs per SM. K1: two tiles per warp, gate and up
+// boxes of 16 rows x 8 superblocks, two stages. K2, one or two tokens: one tile
+// per warp, boxes of 16 rows x 8 superblocks, three stages, and K left unsplit
+// when the row units fill half the CTA slots (no chunk sum follows); three to
+// eight tokens: two tiles per warp, boxes of 64 rows x 4 superblocks, two stages.
 template <bool GATEUP, int MT> struct ShapeQ8;
 template <int MT> struct ShapeQ8<true, MT> {
   static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2;
 };
 template <int MT> struct ShapeQ8<false, MT> {
-  static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 2, CPS = 2;
+  static constexpr int COMBOS = MT <= 2 ? 1 : 4, TPW = MT <= 2 ? 1 : 2, SLICES = MT <= 2 ? 8 : 4,
+                       STAGES = MT <= 2 ? 3 : 2, CPS = 2;
 };
 
 template <bool GATEUP, int MT>
@@ -563,7 +566,8 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
   const int nru1 = (int)(inter / 16), nru2 = (int)(hidden / (16 * cb2));
   const int max_nks = m <= 4 ? 16 : 8;
   choose_split((nsb1 + sl1 - 1) / sl1, nru1, num_sms * cps1, max_nks, &p->nks1, &p->kc1);
-  choose_split((nsb2 + sl2 - 1) / sl2, nru2, num_sms * cps2, max_nks, &p->nks2, &p->kc2);
+  choose_split((nsb2 + sl2 - 1) / sl2, nru2, num_sms * cps2, (p->mt <= 2 && 2 * nru2 >= num_sms * cps2) ? 1 : max_nks,
+               &p->nks2, &p->kc2);
   p->grid1 = (int)std::min<int64_t>((int64_t)num_sms * cps1, (int64_t)p->nks1 * nru1);
   p->grid2 = (int)std::min<int64_t>((int64_t)num_sms * cps2, (int64_t)p->nks2 * nru2);
   size_t o = 0;
