@@ -499,12 +499,13 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 // the other's arithmetic); K1 two stages; K2 one 16-row tile per unit and warp
 // (boxes of 16 rows x 8 superblocks, three stages), which gives enough units to
 // leave K unsplit on large layers, so no chunk sum follows. 5-8 tokens (two
-// token tiles, twice the registers for B): one CTA per SM, four stages, K2 boxes
-// of 64 rows x 4 superblocks.
+// token tiles, twice the registers for B): one CTA per SM; K1 one tile per warp
+// (gate or up), boxes of 16 rows x 4 superblocks, two stages; K2 boxes of 64
+// rows x 4 superblocks, four stages.
 template <bool GATEUP, int NT> struct Shape;
 template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
 template <> struct Shape<false, 1> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 8, STAGES = 3, CPS = 2; };
-template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 4, CPS = 1; };
+template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 2, CPS = 1; };
 template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4, CPS = 1; };
 
 template <bool GATEUP, int NT>
