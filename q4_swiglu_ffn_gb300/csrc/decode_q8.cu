@@ -447,14 +447,15 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes: 8 warps, two CTAs per SM. K1: two tiles per warp, gate and up
-// boxes of 16 rows x 8 superblocks, two stages. K2, one or two tokens: one tile
+// CTA shapes: 8 warps, two CTAs per SM. K1: gate and up boxes, two stages; one or
+// two tokens: two tiles per warp, 8 superblocks per step; three to eight tokens:
+// one tile per warp (fewer registers for the MMA path), 4 superblocks per step. K2, one or two tokens: one tile
 // per warp, boxes of 16 rows x 8 superblocks, three stages, and K left unsplit
 // when the row units fill half the CTA slots (no chunk sum follows); three to
 // eight tokens: two tiles per warp, boxes of 64 rows x 4 superblocks, two stages.
 template <bool GATEUP, int MT> struct ShapeQ8;
 template <int MT> struct ShapeQ8<true, MT> {
-  static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2;
+  static constexpr int COMBOS = 2, TPW = MT <= 2 ? 2 : 1, SLICES = MT <= 2 ? 8 : 4, STAGES = 2, CPS = 2;
 };
 template <int MT> struct ShapeQ8<false, MT> {
   static constexpr int COMBOS = MT <= 2 ? 1 : 4, TPW = MT <= 2 ? 1 : 2, SLICES = MT <= 2 ? 8 : 4,
