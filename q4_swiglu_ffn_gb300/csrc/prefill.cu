@@ -5,7 +5,9 @@
 //   P2 mmq<gate/up>        G = deq(Wg) . deq(xq), U = deq(Wu) . deq(xq) on tcgen05,
 //                          h = silu(G) * U, h -> planar Q8_1 (hq)
 //   P3 expand(hq)
-//   P4 mmq<down>           y = deq(Wd) . deq(hq), float32
+//   P4 mmq<down>           y = deq(Wd) . deq(hq), float32 (at small m split into K slices
+//                          that fill one wave, each writing partial sums)
+//   P5 finish_down         the slices' sum in slice order, and/or y stored as bf16 (only then)
 // Source: spark_model/layers/ops/q4k_mmq.rs (per-prefill activations to Q8_1,
 // then the Q4_K MMQ GEMM C[m, n] = A_q8[m, k] x W_q4k[n, k]); realizar
 // layers/ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (x quantized to Q8_1 once for
