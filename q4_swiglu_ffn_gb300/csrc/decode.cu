@@ -310,8 +310,10 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = 0.f;
   // A warp keeps the B fragments of its superblock in registers for as long as
   // that superblock stays the same (with one group per K-chunk: until its chunk
-  // changes).
-  uint2 bc[16][NT];
+  // changes). With two token tiles they take 64 registers, which leave no room
+  // for two CTAs per SM; there they are read through L1 at each use.
+  constexpr bool CACHEB = NT == 1 || CPS == 1;
+  uint2 bc[CACHEB ? 16 : 1][NT];
   uint32_t bmc[NT];
   float xsc[NT];
   int csb = -1;
@@ -378,12 +380,14 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         for (int n = 0; n < NT; ++n)
 #pragma unroll
           for (int i = 0; i < 4; ++i) c[t][n][0][i] = c[t][n][1][i] = cm[t][n][i] = 0.f;
+      const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
       if (sb != csb) {
-        const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
+        if constexpr (CACHEB) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
+          for (int k = 0; k < 16; ++k)
 #pragma unroll
-          for (int n = 0; n < NT; ++n) bc[k][n] = fx[(k * NT + n) * 32 + flane[n]];
+            for (int n = 0; n < NT; ++n) bc[k][n] = fx[(k * NT + n) * 32 + flane[n]];
+        }
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           bmc[n] = P.in.fm[((int64_t)sb * NT + n) * 32 + flane[n]];
@@ -396,8 +400,13 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         uint2 b0[NT], b1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-          b0[n] = bc[2 * w][n];
-          b1[n] = bc[2 * w + 1][n];
+          if constexpr (CACHEB) {
+            b0[n] = bc[2 * w][n];
+            b1[n] = bc[2 * w + 1][n];
+          } else {
+            b0[n] = __ldg(fx + (2 * w * NT + n) * 32 + flane[n]);
+            b1[n] = __ldg(fx + ((2 * w + 1) * NT + n) * 32 + flane[n]);
+          }
         }
 #pragma unroll
         for (int t = 0; t < TPW; ++t) {
@@ -493,20 +502,22 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes: 8 warps. K1: two tiles per warp (gate and up of the same rows)
-// sharing the B operand, gate and up boxes of 16 rows x 8 superblocks. Up to 4
-// tokens: two CTAs per SM (they drift apart, so one's loads and waits overlap
-// the other's arithmetic); K1 two stages; K2 one 16-row tile per unit and warp
-// (boxes of 16 rows x 8 superblocks, three stages), which gives enough units to
-// leave K unsplit on large layers, so no chunk sum follows. 5-8 tokens (two
-// token tiles, twice the registers for B): one CTA per SM; K1 one tile per warp
-// (gate or up), boxes of 16 rows x 4 superblocks, two stages; K2 boxes of 64
-// rows x 4 superblocks, four stages.
+// CTA shapes. Up to 4 tokens, 8 warps and two CTAs per SM (they drift apart, so
+// one's loads and waits overlap the other's arithmetic): K1 two tiles per warp
+// (gate and up of the same rows) sharing the B operand, gate and up boxes of 16
+// rows x 8 superblocks, two stages; K2 one 16-row tile per unit and warp (boxes
+// of 16 rows x 8 superblocks, three stages), which gives enough units to leave K
+// unsplit on large layers, so no chunk sum follows. 5-8 tokens (two token tiles;
+// B read through L1, so that a thread fits in 128 registers): small CTAs, many
+// per SM, which keeps 16 warps per SM without tying them to one CTA barrier per
+// step; K1 4 warps (gate or up tile at 2 superblocks), boxes of 16 rows x 2
+// superblocks, two stages, four CTAs per SM; K2 2 warps, boxes of 16 rows x 2
+// superblocks, three stages, eight CTAs per SM.
 template <bool GATEUP, int NT> struct Shape;
 template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2; };
 template <> struct Shape<false, 1> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 8, STAGES = 3, CPS = 2; };
-template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 4, STAGES = 2, CPS = 1; };
-template <> struct Shape<false, 2> { static constexpr int COMBOS = 4, TPW = 2, SLICES = 4, STAGES = 4, CPS = 1; };
+template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 2, STAGES = 2, CPS = 4; };
+template <> struct Shape<false, 2> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 2, STAGES = 3, CPS = 8; };
 
 template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
