@@ -74,6 +74,7 @@ struct PrefillPlan {
   size_t off_xop, off_hop;  // tensor-core operands
   size_t off_misc;
   int ksplit;             // K slices of the down projection
+  int num_sms;            // SMs (resident CTAs of the GEMMs, for their tile order)
   size_t off_ypart;       // their partial outputs [ksplit][m][hidden] (ksplit > 1)
 };
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);

@@ -17,8 +17,9 @@
 // integer kind on sm_103a, so the Q4_K x Q8_1 products run on tcgen05.mma
 // kind::f16 with operands that carry the integers exactly:
 //   A (weights, M = 128 rows):  q * scale_j as fp16 (<= 945, exact), unpacked from
-//                               the 4-bit quants by transform warps straight into
-//                               the 128-byte-swizzled shared-memory layout.
+//                               the 4-bit quants by transform warps and stored
+//                               straight into tensor memory (row i in TMEM lane i),
+//                               so the weights never pass through shared memory.
 //   B (activations, N = 128):   v = q8 * d8 * 2^-e_t split into fp16 hi and lo
 //                               (about 22 bits of v; e_t per token keeps |v| < 2^15).
 // Each superblock (256 k) accumulates into its own TMEM buffer; the epilogue
@@ -127,10 +128,13 @@ constexpr int KCH = 64;                   // k per chunk (one 128-byte swizzle a
 constexpr int CH_PER_SB = 5;              // 4 main chunks + 1 min chunk per superblock
 constexpr int STAGES = 4;
 constexpr int TILE_BYTES = TM * KCH * 2;  // 16 KB
-constexpr int STAGE_BYTES = 3 * TILE_BYTES;
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // B hi and lo; A of the stage is in TMEM
 constexpr int NWARPS = 10;                // 0 TMA, 1 MMA, 2-5 transform, 6-9 epilogue
 constexpr int W_TMA = 0, W_MMA = 1, W_XF = 2, W_EPI = 6;
-constexpr uint32_t TMEM_COLS = 512;       // D_main[2] at 0/128, D_min[2] at 256/384
+// TMEM columns: D_main[2] at 0/128 (fp32), D_min at 256, the A tile of stage s at
+// 384 + 32 s (64 fp16 per lane, two to a column)
+constexpr uint32_t TMEM_COLS = 512, TM_DMIN = 256, TM_A = 384, A_COLS = KCH / 2;
+static_assert(TM_A + STAGES * A_COLS <= TMEM_COLS, "A stages fit in TMEM");
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct MmqParams {
@@ -141,6 +145,7 @@ struct MmqParams {
   int ldo;             // output row length (inter for hq, hidden for y)
   int ntn;             // tiles along N (tokens)
   int ksplit;          // slices of K: CTA b takes slice b / (gridDim / ksplit) (down only; 1 for gate/up)
+  int mt_fast;         // consecutive CTAs take consecutive row tiles (else consecutive token tiles)
   const float* tscale; // 2^e_t per token
   int8_t* hq_qs;       // gate/up: Q8_1 quants of h [m][inter]
   float2* hq_ds;       // gate/up: Q8_1 (d, s) of h [m][inter/32]
@@ -156,11 +161,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 // kind::f16, fp16 A and B, fp32 D, both K-major, N = TN, M = TM
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TN >> 3) << 17) | ((uint32_t)(TM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
+// D (+)= A . B with A read from tensor memory (128 lanes = rows, K along the
+// columns) and B from a shared-memory descriptor
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t acc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(IDESC), "r"(acc));
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(IDESC), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
@@ -180,6 +187,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Each lane stores 32 (8) consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
   asm volatile(
@@ -282,7 +306,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = SPLIT ? (int)gridDim.x / P.ksplit : (int)gridDim.x;  // (row tile, token tile) pairs
   const int ks = SPLIT ? (int)blockIdx.x / tiles : 0, tile = (int)blockIdx.x - ks * tiles;
-  const int nt = tile % P.ntn, mt = tile / P.ntn;
+  const int nmt = tiles / P.ntn;
+  const int nt = P.mt_fast ? tile / nmt : tile % P.ntn, mt = P.mt_fast ? tile % nmt : tile / P.ntn;
   // this CTA's superblocks [sb0, sb0 + nsbl); the loops below count from 0
   const int sb0 = SPLIT ? (int)((int64_t)P.nsb * ks / P.ksplit) : 0;
   const int nsbl = SPLIT ? (int)((int64_t)P.nsb * (ks + 1) / P.ksplit) - sb0 : P.nsb;
@@ -322,11 +347,11 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         const int sb = sb0 + q / CH_PER_SB, c = q % CH_PER_SB;
         if (c < 4) {
           mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
-          tma_load_2d(st + TILE_BYTES, &tm_hi, sb * QK + c * KCH, nt * TN, &full[s]);
-          tma_load_2d(st + 2 * TILE_BYTES, &tm_lo, sb * QK + c * KCH, nt * TN, &full[s]);
+          tma_load_2d(st, &tm_hi, sb * QK + c * KCH, nt * TN, &full[s]);
+          tma_load_2d(st + TILE_BYTES, &tm_lo, sb * QK + c * KCH, nt * TN, &full[s]);
         } else {
           mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-          tma_load_2d(st + TILE_BYTES, &tm_mn, sb * KCH, nt * TN, &full[s]);
+          tma_load_2d(st, &tm_mn, sb * KCH, nt * TN, &full[s]);
         }
       }
     }
@@ -337,23 +362,29 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         const int ab = sb & 1;
         if (sb >= 2 && !wait_bar(&acce[ab], ((sb - 2) >> 1) & 1, abort_flag, P.err)) break;
         tc_fence_after();
-        const uint32_t d_main = tmem + ab * TN, d_min = tmem + 256 + ab * TN;
+        const uint32_t d_main = tmem + ab * TN, d_min = tmem + TM_DMIN;
         bool ok = true;
         for (int c = 0; c < CH_PER_SB; ++c) {
           const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
           if (!wait_bar(&full[s], u & 1, abort_flag, P.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-          const uint64_t a = sw128_desc(st), b0 = sw128_desc(st + TILE_BYTES), b1 = sw128_desc(st + 2 * TILE_BYTES);
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES), a = tmem + TM_A + s * A_COLS;
+          const uint64_t b0 = sw128_desc(st), b1 = sw128_desc(st + TILE_BYTES);
           if (c < 4) {
 #pragma unroll
             for (int ks = 0; ks < KCH / 16; ++ks) {
               const uint64_t off = (uint64_t)((ks * 32) >> 4);  // 16 fp16 = 32 bytes along K
-              mma_f16(d_main, a + off, b0 + off, (c | ks) != 0);
-              mma_f16(d_main, a + off, b1 + off, 1u);
+              mma_f16_ts(d_main, a + ks * 8, b0 + off, (c | ks) != 0);  // 16 fp16 = 8 TMEM columns
+              mma_f16_ts(d_main, a + ks * 8, b1 + off, 1u);
             }
           } else {
-            mma_f16(d_min, a, b0, 0u);
+            // D_min has one buffer: the epilogue must have read the previous superblock's
+            if (sb >= 1 && !wait_bar(&acce[(sb - 1) & 1], ((sb - 1) >> 1) & 1, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            mma_f16_ts(d_min, a, b0, 0u);
           }
           mma_commit(&empty[s]);
         }
@@ -362,16 +393,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       }
     }
   } else if (warp < W_EPI) {
-    // ------------------------------------------------------------ transform: Q4_K -> fp16 A tiles
-    const int r = threadIdx.x - W_XF * 32;  // tile row 0..127
+    // ------------------------------------------------------------ transform: Q4_K -> fp16 A tiles in TMEM
+    // A warp reaches TMEM lanes 32 * (warp % 4) .. +31 only, so that quarter of the rows is its own.
+    const int r = (warp & 3) * 32 + lane;  // tile row 0..127 = TMEM lane
     const uint8_t* src;
     if (GATEUP)
       src = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
     else
       src = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
     src += (int64_t)sb0 * BLK;
-    const uint32_t rsw = (uint32_t)(r & 7);
-    uint8_t* arow_base = smem + (r >> 3) * 1024 + (r & 7) * 128;  // + stage offset
+    const uint32_t a_lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A;  // + stage columns
     uint4 raw[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
@@ -392,39 +423,41 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       for (int c = 0; c < CH_PER_SB; ++c) {
         const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
         if (!ok || (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err))) { ok = false; break; }
-        uint8_t* arow = arow_base + s * STAGE_BYTES;
+        tc_fence_after();  // the MMAs that read this stage have completed
+        const uint32_t arow = a_lanes + s * A_COLS;
         if (c < 4) {
           const __half2 mlo = __float2half2_rn((float)scs[2 * c]), alo = __float2half2_rn(-1024.f * (float)scs[2 * c]);
           const __half2 mhi = __float2half2_rn((float)scs[2 * c + 1] * 0.0625f),
                         ahi = __float2half2_rn(-64.f * (float)scs[2 * c + 1]);
           const uint4 ga = cur[1 + 2 * c], gb = cur[2 + 2 * c];
           const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+          // column j of the row holds k = 2j, 2j + 1: 32 low-nibble k, then 32 high-nibble k
+          uint32_t a[32];
 #pragma unroll
           for (int p = 0; p < 4; ++p) {
             const uint32_t w0 = wds[2 * p], w1 = wds[2 * p + 1];
             const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
-            uint4 lo4, hi4;
-            lo4.x = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            lo4.y = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            lo4.z = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            lo4.w = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            hi4.x = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            hi4.y = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            hi4.z = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            hi4.w = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            *reinterpret_cast<uint4*>(arow + (((uint32_t)p ^ rsw) << 4)) = lo4;
-            *reinterpret_cast<uint4*>(arow + (((uint32_t)(4 + p) ^ rsw) << 4)) = hi4;
+            a[4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            a[4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            a[4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            a[4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+            a[16 + 4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            a[16 + 4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            a[16 + 4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            a[16 + 4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
           }
+          tmem_st32(arow, a);
         } else {
-          uint4 v;
-          v.x = h2_as_u32(__halves2half2(__uint2half_rn(mns[0]), __uint2half_rn(mns[1])));
-          v.y = h2_as_u32(__halves2half2(__uint2half_rn(mns[2]), __uint2half_rn(mns[3])));
-          v.z = h2_as_u32(__halves2half2(__uint2half_rn(mns[4]), __uint2half_rn(mns[5])));
-          v.w = h2_as_u32(__halves2half2(__uint2half_rn(mns[6]), __uint2half_rn(mns[7])));
-          *reinterpret_cast<uint4*>(arow + ((0u ^ rsw) << 4)) = v;
-          *reinterpret_cast<uint4*>(arow + ((1u ^ rsw) << 4)) = v;
+          // the 8 mins twice (k 0-7 against the hi sums, k 8-15 against the lo sums)
+          uint32_t v[8];
+          v[0] = v[4] = h2_as_u32(__halves2half2(__uint2half_rn(mns[0]), __uint2half_rn(mns[1])));
+          v[1] = v[5] = h2_as_u32(__halves2half2(__uint2half_rn(mns[2]), __uint2half_rn(mns[3])));
+          v[2] = v[6] = h2_as_u32(__halves2half2(__uint2half_rn(mns[4]), __uint2half_rn(mns[5])));
+          v[3] = v[7] = h2_as_u32(__halves2half2(__uint2half_rn(mns[6]), __uint2half_rn(mns[7])));
+          tmem_st8(arow, v);
         }
-        fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[s]);
       }
@@ -455,7 +488,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
       if (!wait_bar(&accf[ab], (sb >> 1) & 1, abort_flag, P.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t tm_main = tmem + lane_addr + ab * TN, tm_min = tmem + lane_addr + 256 + ab * TN;
+      const uint32_t tm_main = tmem + lane_addr + ab * TN, tm_min = tmem + lane_addr + TM_DMIN;
 #pragma unroll
       for (int j = 0; j < TN / 16; ++j) {
         float v[16], w[16];
@@ -542,6 +575,19 @@ struct Operand {
   float* scale;
 };
 
+// The CTAs resident at once (one per SM) share operands through L2. Walking token
+// tiles fastest keeps few weight row tiles but every token tile's B planes in
+// flight; walking row tiles fastest the reverse. Take the order whose resident
+// operands are fewer bytes (at large m the down projection's B planes alone
+// exceed L2 in the first order).
+int row_tiles_fastest(int64_t nmt, int64_t ntn, int64_t k, int num_sms) {
+  const int64_t w_tile = (int64_t)TM * (k / QK) * BLK, b_tile = (int64_t)TN * k * 4;
+  const int64_t r = num_sms;
+  const int64_t tok_fast = std::min<int64_t>(nmt, (r + ntn - 1) / ntn) * w_tile + std::min<int64_t>(ntn, r) * b_tile;
+  const int64_t row_fast = std::min<int64_t>(nmt, r) * w_tile + std::min<int64_t>(ntn, (r + nmt - 1) / nmt) * b_tile;
+  return row_fast < tok_fast ? 1 : 0;
+}
+
 }  // namespace
 
 // K slices of the down projection: its (row tile, token tile) CTAs number only
@@ -578,6 +624,7 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   p->off_hop = take(op_bytes(inter, true));
   p->off_misc = take(256);
   p->ksplit = down_ksplit(m, hidden, inter, num_sms);
+  p->num_sms = num_sms;
   p->off_ypart = take((size_t)p->ksplit * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
@@ -631,6 +678,7 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.ldo = (int)I;
   g.ntn = ntn;
   g.ksplit = 1;
+  g.mt_fast = row_tiles_fastest(I / 64, ntn, H, p.num_sms);
   g.tscale = xo.scale;
   g.hq_qs = hq;
   g.hq_ds = hds;
@@ -652,6 +700,7 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.ldo = (int)H;
   dn.ntn = ntn;
   dn.ksplit = p.ksplit;
+  dn.mt_fast = row_tiles_fastest(H / TM, ntn, I, p.num_sms);
   dn.tscale = ho.scale;
   float* ypart = (float*)(W + p.off_ypart);
   const bool fin = p.ksplit > 1 || ybf16;  // the slice sum and/or the bf16 store
