@@ -462,6 +462,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int n = 0; n < NT; ++n) slot[(t * NT + n) * 2] = acc[t][n][0], slot[(t * NT + n) * 2 + 1] = acc[t][n][1];
+      __syncwarp();
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
       if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
         // owner: sum the SLICES partial dot products of every tile and store this chunk's sums

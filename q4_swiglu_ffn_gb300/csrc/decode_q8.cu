@@ -407,6 +407,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
               if ((k & 3) == tig) slot[(t * MT + k) * 2 + r] = v;
             }
       }
+      __syncwarp();
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
       if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
         // owner: sum the SLICES partial dot products of every tile and store this chunk's sums

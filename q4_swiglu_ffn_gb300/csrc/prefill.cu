@@ -135,6 +135,7 @@ constexpr int W_TMA = 0, W_MMA = 1, W_XF = 2, W_EPI = 6;
 // 384 + 32 s (64 fp16 per lane, two to a column)
 constexpr uint32_t TMEM_COLS = 512, TM_DMIN = 256, TM_A = 384, A_COLS = KCH / 2;
 static_assert(TM_A + STAGES * A_COLS <= TMEM_COLS, "A stages fit in TMEM");
+static_assert((TM * (TN + 1) + TN) * 4 <= STAGES * STAGE_BYTES, "the gate/up exchange fits in the stages");
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct MmqParams {
@@ -228,64 +229,59 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z). Below z = -80, e^-z > 5.5e34 and the quotient is z * e^z
+// to within 1e-35 relative; it is computed that way because a divisor beyond 2^126
+// sends the IEEE division down its slow path (and e^-z overflows to inf below -88.7).
+__device__ __forceinline__ float silu_f(float z) { return z < -80.f ? z * expf(z) : z / (1.0f + expf(-z)); }
 
 // SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7).
 // xg holds, per tile row (0-63 gate, 64-127 up, same 64 inter indices), the
-// 128 token columns already multiplied by 2^e_t. Item i = (token i/2, Q8_1
-// block i%2 of 32 inter rows); each warp takes items ew, ew+8, ... four at a
-// time so the shuffle and division chains of independent items overlap.
+// 128 token columns; ts (after xg) their factors 2^e_t. Each of the 256 threads
+// owns one item (token e % 128, Q8_1 block e / 128 of 32 inter rows) whole: its
+// 32 values are independent, so the max and the sum need no shuffles, and its 32
+// quants leave as two 16-byte stores. Reading column tt of a row, the lanes of a
+// warp hit consecutive banks (the row pitch is 129 words).
 __device__ __forceinline__ void gateup_final(const uint8_t* smem, const MmqParams& P, int mt, int nt, int ew,
                                              int lane, volatile int* abort_flag) {
   if (*abort_flag) return;
   const float* xg = reinterpret_cast<const float*>(smem);
   constexpr int LD = TN + 1;
-  const int t0 = nt * TN;
-  for (int base = ew; base < 2 * TN; base += 32) {
-    float h[4];
-    int tt[4], qb[4];
+  const float* ts = xg + TM * LD;
+  const int e = ew * 32 + lane, tt = e & (TN - 1), qb = e / TN;
+  const int t = nt * TN + tt;
+  if (t >= P.m) return;
+  const float sc = ts[tt];
+  float h[Q8B], amax = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int item = base + 8 * k;
-      tt[k] = item >> 1;
-      qb[k] = item & 1;
-      const float g = xg[(qb[k] * 32 + lane) * LD + tt[k]];
-      const float u = xg[(64 + qb[k] * 32 + lane) * LD + tt[k]];
-      h[k] = silu_f(g) * u;
-    }
-    float amax[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) amax[k] = fabsf(h[k]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) amax[k] = fmaxf(amax[k], __shfl_xor_sync(0xffffffffu, amax[k], o));
-    int qi[4], sum[4];
-    float dq[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const bool nz = amax[k] >= 0x1p-120f;  // below: zero block (127/amax would overflow)
-      dq[k] = nz ? __fdiv_rn(amax[k], 127.f) : 0.f;
-      const float inv = nz ? __fdiv_rn(127.f, amax[k]) : 0.f;
-      float rq = roundf(__fmul_rn(h[k], inv));
-      rq = fminf(fmaxf(rq, -127.f), 127.f);
-      qi[k] = (int)rq;
-      sum[k] = qi[k];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sum[k] += __shfl_xor_sync(0xffffffffu, sum[k], o);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int t = t0 + tt[k];
-      if (t < P.m) {
-        const int irow = mt * 64 + qb[k] * 32 + lane;
-        P.hq_qs[(int64_t)t * P.ldo + irow] = (int8_t)qi[k];
-        if (lane == 0) P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq[k], __fmul_rn(dq[k], (float)sum[k]));
-      }
-    }
+  for (int j = 0; j < Q8B; ++j) {
+    const float g = xg[(qb * 32 + j) * LD + tt] * sc;
+    const float u = xg[(64 + qb * 32 + j) * LD + tt] * sc;
+    h[j] = silu_f(g) * u;
+    amax = fmaxf(amax, fabsf(h[j]));
   }
+  const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
+  const float dq = nz ? __fdiv_rn(amax, 127.f) : 0.f;
+  const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
+  int sum = 0;
+  uint32_t pk[Q8B / 4];
+#pragma unroll
+  for (int w = 0; w < Q8B / 4; ++w) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float rq = roundf(__fmul_rn(h[4 * w + b], inv));
+      rq = fminf(fmaxf(rq, -127.f), 127.f);
+      const int qi = (int)rq;
+      sum += qi;
+      v |= ((uint32_t)qi & 0xFFu) << (8 * b);
+    }
+    pk[w] = v;
+  }
+  const int irow = mt * 64 + qb * 32;
+  uint4* dst = reinterpret_cast<uint4*>(P.hq_qs + (int64_t)t * P.ldo + irow);  // 32-byte aligned
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq, __fmul_rn(dq, (float)sum));
 }
 
 // SPLIT: the CTAs of each (row tile, token tile) split K into P.ksplit slices
@@ -332,6 +328,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
+  __syncwarp();  // every CTA or named barrier below is entered by whole warps
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -464,6 +461,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     }
     if (GATEUP) {
       // join the epilogue warps for the SwiGLU + Q8_1 pass over the finished tile
+      __syncwarp();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       gateup_final(smem, P, mt, nt, warp - W_XF, lane, abort_flag);
     }
@@ -506,18 +504,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     if (GATEUP) {
       // exchange through the idle stage buffers: rows 0-63 hold gate, 64-127 up,
       // for the same 64 inter indices. Every epilogue warp reaches the barrier.
-      float* xg = reinterpret_cast<float*>(smem);  // [128 rows][TN + 1]
+      float* xg = reinterpret_cast<float*>(smem);  // [128 rows][TN + 1], then the 128 token factors
       constexpr int LD = TN + 1;
       if (ok) {
 #pragma unroll
-        for (int i = 0; i < TN; ++i) {
-          const int t = t0 + i;
-          const float sc = t < P.m ? P.tscale[t] : 0.f;
-          xg[r * LD + i] = acc[i] * sc;
-        }
+        for (int i = 0; i < TN; ++i) xg[r * LD + i] = acc[i];
+        xg[TM * LD + r] = t0 + r < P.m ? P.tscale[t0 + r] : 0.f;  // thread r brings token r's factor
       } else {
         *abort_flag = 1;
       }
+      __syncwarp();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       gateup_final(smem, P, mt, nt, 4 + (warp - W_EPI), lane, abort_flag);
     } else if (ok) {
@@ -531,7 +527,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     }
   }
   // ---------------------------------------------------------------- teardown
+  // (lane 0 of the TMA and MMA warps arrives after its loop, the other lanes long before)
   tc_fence_before();
+  __syncwarp();
   __syncthreads();
   if (*abort_flag) {
     // let copies and MMAs already in flight land before the shared memory and TMEM go away

@@ -341,6 +341,7 @@ __global__ void __launch_bounds__(Q6_WARPS * 32, CPS) q6k_gemv_kernel(const Q6Pa
     float* slot = red + ((size_t)warp * 32 + lane) * NT * 2;
 #pragma unroll
     for (int n = 0; n < NT; ++n) slot[2 * n] = acc[n][0], slot[2 * n + 1] = acc[n][1];
+    __syncwarp();
     __syncthreads();
     if (warp == (tile & (Q6_WARPS - 1)) && !*abort_flag) {
 #pragma unroll
