@@ -129,14 +129,15 @@ constexpr int CH_PER_SB = 5;              // 4 main chunks + 1 min chunk per sup
 constexpr int STAGES = 4;
 constexpr int TILE_BYTES = TM * KCH * 2;  // 16 KB
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // B hi and lo; A of the stage is in TMEM
-constexpr int NWARPS = 10;                // 0 TMA, 1 MMA, 2-5 transform, 6-9 epilogue
-constexpr int W_TMA = 0, W_MMA = 1, W_XF = 2, W_EPI = 6;
+constexpr int NWARPS = 14;                // 0 TMA, 1 MMA, 2-5 transform, 6-13 epilogue
+constexpr int W_TMA = 0, W_MMA = 1, W_EPI = 6, N_EPI = 8;  // warps W_MMA + 1 .. W_EPI - 1 transform
 // TMEM columns: D_main[2] at 0/128 (fp32), D_min at 256, the A tile of stage s at
 // 384 + 32 s (64 fp16 per lane, two to a column)
 constexpr uint32_t TMEM_COLS = 512, TM_DMIN = 256, TM_A = 384, A_COLS = KCH / 2;
 static_assert(TM_A + STAGES * A_COLS <= TMEM_COLS, "A stages fit in TMEM");
-static_assert((TM * (TN + 1) + TN) * 4 <= STAGES * STAGE_BYTES, "the gate/up exchange fits in the stages");
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+// gate/up exchange: [128 rows][TN + 1] raw sums, then the TN token factors 2^e_t
+constexpr int XG_BYTES = (TM * (TN + 1) + TN) * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XG_BYTES + 1024 /*align*/ + 256 /*barriers*/;
 
 struct MmqParams {
   const uint8_t* w0;   // gate (gate/up kernel) or down
@@ -145,7 +146,9 @@ struct MmqParams {
   int m;               // tokens
   int ldo;             // output row length (inter for hq, hidden for y)
   int ntn;             // tiles along N (tokens)
-  int ksplit;          // slices of K: CTA b takes slice b / (gridDim / ksplit) (down only; 1 for gate/up)
+  int ksplit;          // slices of K (down only; 1 for gate/up)
+  int tiles;           // (row tile, token tile) pairs
+  int nwork;           // work items: tiles x ksplit; item w is slice w / tiles of tile w % tiles
   int mt_fast;         // consecutive CTAs take consecutive row tiles (else consecutive token tiles)
   const float* tscale; // 2^e_t per token
   int8_t* hq_qs;       // gate/up: Q8_1 quants of h [m][inter]
@@ -230,9 +233,12 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
 }
 
 // silu(z) = z / (1 + e^-z). Below z = -80, e^-z > 5.5e34 and the quotient is z * e^z
-// to within 1e-35 relative; it is computed that way because a divisor beyond 2^126
-// sends the IEEE division down its slow path (and e^-z overflows to inf below -88.7).
-__device__ __forceinline__ float silu_f(float z) { return z < -80.f ? z * expf(z) : z / (1.0f + expf(-z)); }
+// to within 1e-35 relative. Above, the divisor is below 2^126, where CUDA's __fdividef
+// is within 2 ulp and has no branch (the IEEE division's slow-path branch kept the
+// 32 independent values of an item from overlapping).
+__device__ __forceinline__ float silu_f(float z) {
+  return z < -80.f ? z * expf(z) : __fdividef(z, 1.0f + expf(-z));
+}
 
 // SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7).
 // xg holds, per tile row (0-63 gate, 64-127 up, same 64 inter indices), the
@@ -241,10 +247,9 @@ __device__ __forceinline__ float silu_f(float z) { return z < -80.f ? z * expf(z
 // 32 values are independent, so the max and the sum need no shuffles, and its 32
 // quants leave as two 16-byte stores. Reading column tt of a row, the lanes of a
 // warp hit consecutive banks (the row pitch is 129 words).
-__device__ __forceinline__ void gateup_final(const uint8_t* smem, const MmqParams& P, int mt, int nt, int ew,
+__device__ __forceinline__ void gateup_final(const float* xg, const MmqParams& P, int mt, int nt, int ew,
                                              int lane, volatile int* abort_flag) {
   if (*abort_flag) return;
-  const float* xg = reinterpret_cast<const float*>(smem);
   constexpr int LD = TN + 1;
   const float* ts = xg + TM * LD;
   const int e = ew * 32 + lane, tt = e & (TN - 1), qb = e / TN;
@@ -284,15 +289,18 @@ __device__ __forceinline__ void gateup_final(const uint8_t* smem, const MmqParam
   P.hq_ds[(int64_t)t * (P.ldo / Q8B) + irow / Q8B] = make_float2(dq, __fmul_rn(dq, (float)sum));
 }
 
-// SPLIT: the CTAs of each (row tile, token tile) split K into P.ksplit slices
-// (the down projection at small m); without it every CTA takes all of K.
+// Persistent: one CTA per SM walks the work items blockIdx.x, + gridDim.x, ... with
+// every pipeline (stages, TMEM buffers, their barrier phases) running on across
+// items, so one item's last superblocks and epilogue overlap the next item's first
+// loads and MMAs. SPLIT: the down projection at small m, K split into P.ksplit slices.
 template <bool GATEUP, bool SPLIT>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     mmq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constant__ CUtensorMap tm_lo,
                const __grid_constant__ CUtensorMap tm_mn, const MmqParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  float* xg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + XG_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* accf = empty + STAGES;
   uint64_t* acce = accf + 2;
@@ -300,14 +308,28 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles = SPLIT ? (int)gridDim.x / P.ksplit : (int)gridDim.x;  // (row tile, token tile) pairs
-  const int ks = SPLIT ? (int)blockIdx.x / tiles : 0, tile = (int)blockIdx.x - ks * tiles;
-  const int nmt = tiles / P.ntn;
-  const int nt = P.mt_fast ? tile / nmt : tile % P.ntn, mt = P.mt_fast ? tile % nmt : tile / P.ntn;
-  // this CTA's superblocks [sb0, sb0 + nsbl); the loops below count from 0
-  const int sb0 = SPLIT ? (int)((int64_t)P.nsb * ks / P.ksplit) : 0;
-  const int nsbl = SPLIT ? (int)((int64_t)P.nsb * (ks + 1) / P.ksplit) - sb0 : P.nsb;
+  const int nmt = P.tiles / P.ntn;
   const int64_t rowbytes = (int64_t)P.nsb * BLK;
+  struct Work {
+    int nt, mt, ks, sb0, nsbl;  // token tile, row tile, K slice, its superblocks [sb0, sb0 + nsbl)
+  };
+  auto work = [&](int w) {
+    Work k;
+    k.ks = SPLIT ? w / P.tiles : 0;
+    const int tile = w - k.ks * P.tiles;
+    k.nt = P.mt_fast ? tile / nmt : tile % P.ntn;
+    k.mt = P.mt_fast ? tile % nmt : tile / P.ntn;
+    k.sb0 = SPLIT ? (int)((int64_t)P.nsb * k.ks / P.ksplit) : 0;
+    k.nsbl = SPLIT ? (int)((int64_t)P.nsb * (k.ks + 1) / P.ksplit) - k.sb0 : P.nsb;
+    return k;
+  };
+  // the Q4_K row of tile row r (0-63 gate, 64-127 up for gate/up), at the item's first superblock
+  auto row_ptr = [&](const Work& k, int r) {
+    const uint8_t* p = GATEUP ? (r < 64 ? P.w0 + (int64_t)(k.mt * 64 + r) * rowbytes
+                                        : P.w1 + (int64_t)(k.mt * 64 + r - 64) * rowbytes)
+                              : P.w0 + (int64_t)(k.mt * TM + r) * rowbytes;
+    return p + (int64_t)k.sb0 * BLK;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -315,8 +337,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       mbar_init(&empty[s], 1);  // one tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);   // tcgen05.commit
-      mbar_init(&acce[b], 4);   // 4 epilogue warps
+      mbar_init(&accf[b], 1);      // tcgen05.commit
+      mbar_init(&acce[b], N_EPI);  // the epilogue warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -332,197 +354,228 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nchunks = nsbl * CH_PER_SB;
 
   if (warp == W_TMA) {
     // ------------------------------------------------------------ TMA producer (B operand)
     if (lane == 0) {
-      for (int q = 0; q < nchunks; ++q) {
-        const int s = q % STAGES, u = q / STAGES;
-        if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) break;
-        uint8_t* st = smem + s * STAGE_BYTES;
-        const int sb = sb0 + q / CH_PER_SB, c = q % CH_PER_SB;
-        if (c < 4) {
-          mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
-          tma_load_2d(st, &tm_hi, sb * QK + c * KCH, nt * TN, &full[s]);
-          tma_load_2d(st + TILE_BYTES, &tm_lo, sb * QK + c * KCH, nt * TN, &full[s]);
-        } else {
-          mbar_arrive_expect_tx(&full[s], TILE_BYTES);
-          tma_load_2d(st, &tm_mn, sb * KCH, nt * TN, &full[s]);
+      int q = 0;
+      bool ok = true;
+      for (int w = blockIdx.x; w < P.nwork && ok; w += gridDim.x) {
+        const Work k = work(w);
+        for (int sb = 0; sb < k.nsbl && ok; ++sb) {
+          for (int c = 0; c < CH_PER_SB; ++c, ++q) {
+            const int s = q % STAGES, u = q / STAGES;
+            if (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + s * STAGE_BYTES;
+            const int sba = k.sb0 + sb;
+            if (c < 4) {
+              mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
+              tma_load_2d(st, &tm_hi, sba * QK + c * KCH, k.nt * TN, &full[s]);
+              tma_load_2d(st + TILE_BYTES, &tm_lo, sba * QK + c * KCH, k.nt * TN, &full[s]);
+            } else {
+              mbar_arrive_expect_tx(&full[s], TILE_BYTES);
+              tma_load_2d(st, &tm_mn, sba * KCH, k.nt * TN, &full[s]);
+            }
+          }
         }
       }
     }
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      for (int sb = 0; sb < nsbl && !*abort_flag; ++sb) {
-        const int ab = sb & 1;
-        if (sb >= 2 && !wait_bar(&acce[ab], ((sb - 2) >> 1) & 1, abort_flag, P.err)) break;
-        tc_fence_after();
-        const uint32_t d_main = tmem + ab * TN, d_min = tmem + TM_DMIN;
-        bool ok = true;
-        for (int c = 0; c < CH_PER_SB; ++c) {
-          const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
-          if (!wait_bar(&full[s], u & 1, abort_flag, P.err)) { ok = false; break; }
+      int q = 0, G = 0;  // chunks and superblocks issued so far (all items)
+      bool ok = true;
+      for (int w = blockIdx.x; w < P.nwork && ok; w += gridDim.x) {
+        const int nsbl = work(w).nsbl;
+        for (int sb = 0; sb < nsbl && ok; ++sb, ++G) {
+          const int ab = G & 1;
+          if (G >= 2 && !wait_bar(&acce[ab], ((G - 2) >> 1) & 1, abort_flag, P.err)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + s * STAGE_BYTES), a = tmem + TM_A + s * A_COLS;
-          const uint64_t b0 = sw128_desc(st), b1 = sw128_desc(st + TILE_BYTES);
-          if (c < 4) {
-#pragma unroll
-            for (int ks = 0; ks < KCH / 16; ++ks) {
-              const uint64_t off = (uint64_t)((ks * 32) >> 4);  // 16 fp16 = 32 bytes along K
-              mma_f16_ts(d_main, a + ks * 8, b0 + off, (c | ks) != 0);  // 16 fp16 = 8 TMEM columns
-              mma_f16_ts(d_main, a + ks * 8, b1 + off, 1u);
-            }
-          } else {
-            // D_min has one buffer: the epilogue must have read the previous superblock's
-            if (sb >= 1 && !wait_bar(&acce[(sb - 1) & 1], ((sb - 1) >> 1) & 1, abort_flag, P.err)) {
+          const uint32_t d_main = tmem + ab * TN, d_min = tmem + TM_DMIN;
+          for (int c = 0; c < CH_PER_SB; ++c, ++q) {
+            const int s = q % STAGES, u = q / STAGES;
+            if (!wait_bar(&full[s], u & 1, abort_flag, P.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            mma_f16_ts(d_min, a, b0, 0u);
+            const uint32_t st = smem_u32(smem + s * STAGE_BYTES), a = tmem + TM_A + s * A_COLS;
+            const uint64_t b0 = sw128_desc(st), b1 = sw128_desc(st + TILE_BYTES);
+            if (c < 4) {
+#pragma unroll
+              for (int ks = 0; ks < KCH / 16; ++ks) {
+                const uint64_t off = (uint64_t)((ks * 32) >> 4);  // 16 fp16 = 32 bytes along K
+                mma_f16_ts(d_main, a + ks * 8, b0 + off, (c | ks) != 0);  // 16 fp16 = 8 TMEM columns
+                mma_f16_ts(d_main, a + ks * 8, b1 + off, 1u);
+              }
+            } else {
+              // D_min has one buffer: the epilogue must have read the previous superblock's
+              if (G >= 1 && !wait_bar(&acce[(G - 1) & 1], ((G - 1) >> 1) & 1, abort_flag, P.err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              mma_f16_ts(d_min, a, b0, 0u);
+            }
+            mma_commit(&empty[s]);
           }
-          mma_commit(&empty[s]);
+          if (!ok) break;
+          mma_commit(&accf[ab]);
         }
-        if (!ok) break;
-        mma_commit(&accf[ab]);
       }
     }
   } else if (warp < W_EPI) {
     // ------------------------------------------------------------ transform: Q4_K -> fp16 A tiles in TMEM
     // A warp reaches TMEM lanes 32 * (warp % 4) .. +31 only, so that quarter of the rows is its own.
     const int r = (warp & 3) * 32 + lane;  // tile row 0..127 = TMEM lane
-    const uint8_t* src;
-    if (GATEUP)
-      src = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
-    else
-      src = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
-    src += (int64_t)sb0 * BLK;
     const uint32_t a_lanes = tmem + ((uint32_t)((warp & 3) * 32) << 16) + TM_A;  // + stage columns
-    uint4 raw[9];
+    int w = blockIdx.x;
+    if (w < P.nwork) {
+      Work k = work(w);
+      const uint8_t* src = row_ptr(k, r);
+      uint4 raw[9];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
-    bool ok = true;
-    for (int sb = 0; sb < nsbl && ok; ++sb) {
-      uint4 cur[9];
+      for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      int q = 0;
+      bool ok = true;
+      while (ok) {
+        for (int sb = 0; sb < k.nsbl && ok; ++sb) {
+          uint4 cur[9];
 #pragma unroll
-      for (int i = 0; i < 9; ++i) cur[i] = raw[i];
-      if (sb + 1 < nsbl) {
+          for (int i = 0; i < 9; ++i) cur[i] = raw[i];
+          // prefetch the next superblock: of this item, else the first of the next
+          const uint8_t* nxt = nullptr;
+          if (sb + 1 < k.nsbl)
+            nxt = src + (int64_t)(sb + 1) * BLK;
+          else if (w + (int)gridDim.x < P.nwork)
+            nxt = row_ptr(work(w + gridDim.x), r);
+          if (nxt) {
 #pragma unroll
-        for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)(sb + 1) * BLK) + i);
-      }
-      const uint4 hd = cur[0];
-      uint32_t scs[8], mns[8];  // all 6-bit scales and mins of this superblock
-#pragma unroll
-      for (int j = 0; j < 8; ++j) scale_min(hd.y, hd.z, hd.w, j, scs[j], mns[j]);
-#pragma unroll
-      for (int c = 0; c < CH_PER_SB; ++c) {
-        const int q = sb * CH_PER_SB + c, s = q % STAGES, u = q / STAGES;
-        if (!ok || (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err))) { ok = false; break; }
-        tc_fence_after();  // the MMAs that read this stage have completed
-        const uint32_t arow = a_lanes + s * A_COLS;
-        if (c < 4) {
-          const __half2 mlo = __float2half2_rn((float)scs[2 * c]), alo = __float2half2_rn(-1024.f * (float)scs[2 * c]);
-          const __half2 mhi = __float2half2_rn((float)scs[2 * c + 1] * 0.0625f),
-                        ahi = __float2half2_rn(-64.f * (float)scs[2 * c + 1]);
-          const uint4 ga = cur[1 + 2 * c], gb = cur[2 + 2 * c];
-          const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-          // column j of the row holds k = 2j, 2j + 1: 32 low-nibble k, then 32 high-nibble k
-          uint32_t a[32];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint32_t w0 = wds[2 * p], w1 = wds[2 * p + 1];
-            const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
-            a[4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            a[4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            a[4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            a[4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-            a[16 + 4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            a[16 + 4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            a[16 + 4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-            a[16 + 4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+            for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(nxt) + i);
           }
-          tmem_st32(arow, a);
-        } else {
-          // the 8 mins twice (k 0-7 against the hi sums, k 8-15 against the lo sums)
-          uint32_t v[8];
-          v[0] = v[4] = h2_as_u32(__halves2half2(__uint2half_rn(mns[0]), __uint2half_rn(mns[1])));
-          v[1] = v[5] = h2_as_u32(__halves2half2(__uint2half_rn(mns[2]), __uint2half_rn(mns[3])));
-          v[2] = v[6] = h2_as_u32(__halves2half2(__uint2half_rn(mns[4]), __uint2half_rn(mns[5])));
-          v[3] = v[7] = h2_as_u32(__halves2half2(__uint2half_rn(mns[6]), __uint2half_rn(mns[7])));
-          tmem_st8(arow, v);
+          const uint4 hd = cur[0];
+          uint32_t scs[8], mns[8];  // all 6-bit scales and mins of this superblock
+#pragma unroll
+          for (int j = 0; j < 8; ++j) scale_min(hd.y, hd.z, hd.w, j, scs[j], mns[j]);
+#pragma unroll
+          for (int c = 0; c < CH_PER_SB; ++c) {
+            const int s = q % STAGES, u = q / STAGES;
+            ++q;
+            if (!ok || (u > 0 && !wait_bar(&empty[s], (u - 1) & 1, abort_flag, P.err))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();  // the MMAs that read this stage have completed
+            const uint32_t arow = a_lanes + s * A_COLS;
+            if (c < 4) {
+              const __half2 mlo = __float2half2_rn((float)scs[2 * c]), alo = __float2half2_rn(-1024.f * (float)scs[2 * c]);
+              const __half2 mhi = __float2half2_rn((float)scs[2 * c + 1] * 0.0625f),
+                            ahi = __float2half2_rn(-64.f * (float)scs[2 * c + 1]);
+              const uint4 ga = cur[1 + 2 * c], gb = cur[2 + 2 * c];
+              const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+              // column j of the row holds k = 2j, 2j + 1: 32 low-nibble k, then 32 high-nibble k
+              uint32_t a[32];
+#pragma unroll
+              for (int p = 0; p < 4; ++p) {
+                const uint32_t w0 = wds[2 * p], w1 = wds[2 * p + 1];
+                const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
+                a[4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+                a[4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
+                a[4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+                a[4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
+                a[16 + 4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+                a[16 + 4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+                a[16 + 4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+                a[16 + 4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+              }
+              tmem_st32(arow, a);
+            } else {
+              // the 8 mins twice (k 0-7 against the hi sums, k 8-15 against the lo sums)
+              uint32_t v[8];
+              v[0] = v[4] = h2_as_u32(__halves2half2(__uint2half_rn(mns[0]), __uint2half_rn(mns[1])));
+              v[1] = v[5] = h2_as_u32(__halves2half2(__uint2half_rn(mns[2]), __uint2half_rn(mns[3])));
+              v[2] = v[6] = h2_as_u32(__halves2half2(__uint2half_rn(mns[4]), __uint2half_rn(mns[5])));
+              v[3] = v[7] = h2_as_u32(__halves2half2(__uint2half_rn(mns[6]), __uint2half_rn(mns[7])));
+              tmem_st8(arow, v);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&full[s]);
+          }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full[s]);
+        w += gridDim.x;
+        if (w >= P.nwork) break;
+        k = work(w);
+        src = row_ptr(k, r);
       }
-    }
-    if (GATEUP) {
-      // join the epilogue warps for the SwiGLU + Q8_1 pass over the finished tile
-      __syncwarp();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      gateup_final(smem, P, mt, nt, warp - W_XF, lane, abort_flag);
     }
   } else {
-    // ------------------------------------------------------------ epilogue
-    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const int r = quarter * 32 + lane;
-    const uint8_t* hdr;
-    if (GATEUP)
-      hdr = (r < 64 ? P.w0 + (int64_t)(mt * 64 + r) * rowbytes : P.w1 + (int64_t)(mt * 64 + r - 64) * rowbytes);
-    else
-      hdr = P.w0 + (int64_t)(mt * TM + r) * rowbytes;
-    hdr += (int64_t)sb0 * BLK;
-    float acc[TN];
-#pragma unroll
-    for (int i = 0; i < TN; ++i) acc[i] = 0.f;
+    // ------------------------------------------------------------ epilogue (8 warps)
+    // Warp pair (quarter, half): TMEM lanes 32 * quarter .. +31 (tile rows), token
+    // columns 64 * half .. +63. Every epilogue warp walks every item and reaches both
+    // named barriers of each, also after an abort (then without waiting or reading).
+    const int quarter = warp & 3, half = (warp - W_EPI) >> 2;
+    const int r = quarter * 32 + lane, c0 = half * (TN / 2);
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    constexpr int LD = TN + 1;
+    int G = 0;  // superblocks consumed so far (all items)
     bool ok = true;
-    for (int sb = 0; sb < nsbl; ++sb) {
-      const int ab = sb & 1;
-      const uint32_t dm2 = __ldg(reinterpret_cast<const uint32_t*>(hdr + (int64_t)sb * BLK));
-      const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
-      if (!wait_bar(&accf[ab], (sb >> 1) & 1, abort_flag, P.err)) { ok = false; break; }
-      tc_fence_after();
-      const uint32_t tm_main = tmem + lane_addr + ab * TN, tm_min = tmem + lane_addr + TM_DMIN;
+    for (int w = blockIdx.x; w < P.nwork; w += gridDim.x) {
+      const Work k = work(w);
+      const uint8_t* hdr = row_ptr(k, r);
+      float acc[TN / 2];
 #pragma unroll
-      for (int j = 0; j < TN / 16; ++j) {
-        float v[16], w[16];
-        tmem_ld16(tm_main + j * 16, v);
-        tmem_ld16(tm_min + j * 16, w);
-        tmem_wait_ld();
+      for (int i = 0; i < TN / 2; ++i) acc[i] = 0.f;
+      for (int sb = 0; sb < k.nsbl; ++sb, ++G) {
+        const int ab = G & 1;
+        if (!ok) continue;
+        const uint32_t dm2 = __ldg(reinterpret_cast<const uint32_t*>(hdr + (int64_t)sb * BLK));
+        const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
+        ok = __all_sync(0xffffffffu, wait_bar(&accf[ab], (G >> 1) & 1, abort_flag, P.err));
+        if (!ok) continue;
+        tc_fence_after();
+        const uint32_t tm_main = tmem + lane_addr + ab * TN + c0, tm_min = tmem + lane_addr + TM_DMIN + c0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(w[i], dmn, fmaf(v[i], d, acc[j * 16 + i]));
+        for (int j = 0; j < TN / 32; ++j) {
+          float v[16], u[16];
+          tmem_ld16(tm_main + j * 16, v);
+          tmem_ld16(tm_min + j * 16, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(u[i], dmn, fmaf(v[i], d, acc[j * 16 + i]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[ab]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[ab]);
-    }
-    const int t0 = nt * TN;
-    if (GATEUP) {
-      // exchange through the idle stage buffers: rows 0-63 hold gate, 64-127 up,
-      // for the same 64 inter indices. Every epilogue warp reaches the barrier.
-      float* xg = reinterpret_cast<float*>(smem);  // [128 rows][TN + 1], then the 128 token factors
-      constexpr int LD = TN + 1;
-      if (ok) {
+      if (!ok) *abort_flag = 1;
+      const int t0 = k.nt * TN;
+      if (GATEUP) {
+        // rows 0-63 hold gate, 64-127 up, for the same 64 inter indices; the previous
+        // item's SwiGLU pass has finished reading the exchange before it is rewritten
+        __syncwarp();
+        asm volatile("bar.sync 2, 256;" ::: "memory");
 #pragma unroll
-        for (int i = 0; i < TN; ++i) xg[r * LD + i] = acc[i];
-        xg[TM * LD + r] = t0 + r < P.m ? P.tscale[t0 + r] : 0.f;  // thread r brings token r's factor
-      } else {
-        *abort_flag = 1;
-      }
-      __syncwarp();
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      gateup_final(smem, P, mt, nt, 4 + (warp - W_EPI), lane, abort_flag);
-    } else if (ok) {
-      const int row = mt * TM + r;
-      float* yo = P.y + (int64_t)ks * P.m * P.ldo;
+        for (int i = 0; i < TN / 2; ++i) xg[r * LD + c0 + i] = acc[i];
+        if (half == 0) xg[TM * LD + r] = t0 + r < P.m ? P.tscale[t0 + r] : 0.f;  // thread r: token r's factor
+        __syncwarp();
+        asm volatile("bar.sync 2, 256;" ::: "memory");
+        gateup_final(xg, P, k.mt, k.nt, warp - W_EPI, lane, abort_flag);
+      } else if (ok) {
+        const int row = k.mt * TM + r;
+        float* yo = P.y + (int64_t)k.ks * P.m * P.ldo;
 #pragma unroll
-      for (int i = 0; i < TN; ++i) {
-        const int t = t0 + i;
-        if (t < P.m) yo[(int64_t)t * P.ldo + row] = acc[i] * P.tscale[t];
+        for (int i = 0; i < TN / 2; ++i) {
+          const int t = t0 + c0 + i;
+          if (t < P.m) yo[(int64_t)t * P.ldo + row] = acc[i] * P.tscale[t];
+        }
       }
     }
   }
@@ -551,9 +604,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
                  TN, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// One persistent CTA per SM (at most one per work item).
 template <bool GATEUP, bool SPLIT>
 cudaError_t launch_mmq(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& mn, const MmqParams& P,
-                       int grid, cudaStream_t s) {
+                       int num_sms, cudaStream_t s) {
+  const int grid = std::min(P.nwork, num_sms);
   auto kern = mmq_kernel<GATEUP, SPLIT>;
   static uint64_t attr_set = 0;
   int dev = 0;
@@ -677,12 +732,13 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.ntn = ntn;
   g.ksplit = 1;
   g.mt_fast = row_tiles_fastest(I / 64, ntn, H, p.num_sms);
+  g.tiles = g.nwork = (int)(I / 64) * ntn;
   g.tscale = xo.scale;
   g.hq_qs = hq;
   g.hq_ds = hds;
   g.err = err;
   prof.before(2, s);
-  e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, (int)(I / 64) * ntn, s);
+  e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s);
   prof.after(2, s);
   if (e != cudaSuccess) return e;
 
@@ -699,14 +755,16 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.ntn = ntn;
   dn.ksplit = p.ksplit;
   dn.mt_fast = row_tiles_fastest(H / TM, ntn, I, p.num_sms);
+  dn.tiles = (int)(H / TM) * ntn;
+  dn.nwork = dn.tiles * p.ksplit;
   dn.tscale = ho.scale;
   float* ypart = (float*)(W + p.off_ypart);
   const bool fin = p.ksplit > 1 || ybf16;  // the slice sum and/or the bf16 store
   dn.y = fin ? ypart : (float*)y;
   dn.err = err;
   prof.before(4, s);  // the down MMQ, and the sum of its K slices when there are several
-  e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn * p.ksplit, s)
-                   : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, (int)(H / TM) * ntn, s);
+  e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s)
+                   : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s);
   if (e == cudaSuccess && fin) e = launch_finish_down(ypart, p.ksplit, m * H, y, ybf16, s);
   prof.after(4, s);
   return e;
