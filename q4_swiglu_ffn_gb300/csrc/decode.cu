@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "gemv_stream.cuh"
 #include "kernels.h"
+#include "q8_1.cuh"
 
 namespace q4k {
 
@@ -133,21 +134,40 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float v[8]) {
   }
 }
 
+// Q8: x (or h) is first rounded to Q8_1 (blocks of 32 = 4 lanes) and its
+// dequantized values q * d become the B operand, the activations of the Q8_1
+// entry point; the token slot's warp is whole, so the shuffles are safe.
+__device__ __forceinline__ void round_q8_1(float v[8], int8_t q[8], float& d, float& s) {
+  q8_1_block8(v, q, d, s);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = (float)q[i] * d;
+}
+
 // K0: one CTA per superblock of x, one warp per token slot.
-template <typename T>
+template <typename T, bool Q8>
 __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f) {
   pdl_launch_dependents();
   const int t = threadIdx.x >> 5, sb = blockIdx.x, lane = threadIdx.x & 31;
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  if (t < m) load8(x + (int64_t)t * hidden + (int64_t)sb * QK + lane * 8, v);
+  if (t < m) {
+    load8(x + (int64_t)t * hidden + (int64_t)sb * QK + lane * 8, v);
+    if (Q8) {
+      int8_t q[8];
+      float d, s;
+      round_q8_1(v, q, d, s);
+    }
+  }
   frag_token(v, t >= m, t, nt, sb, f);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
 // K1b: one CTA per 256-row block of h, one warp per token slot. Sums the
-// gate/up chunks in order, applies SwiGLU and writes the fragments of h.
-__global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, int m, int inter, int nt, FragPtrs f) {
+// gate/up chunks in order, applies SwiGLU and writes the fragments of h (Q8: of
+// Q8_1(h), whose quants and (d, s) also go to hq [m][inter] and hds [m][inter/32]).
+template <bool Q8>
+__global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, int m, int inter, int nt, FragPtrs f,
+                                     uint8_t* __restrict__ hq, float2* __restrict__ hds) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = threadIdx.x >> 5, sb = blockIdx.x, lane = threadIdx.x & 31;
@@ -167,6 +187,18 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = silu_f(g[i]) * u[i];
+    if (Q8) {
+      int8_t q[8];
+      float d, s;
+      round_q8_1(v, q, d, s);
+      uint2 pk;
+      pk.x = (uint32_t)(uint8_t)q[0] | (uint32_t)(uint8_t)q[1] << 8 | (uint32_t)(uint8_t)q[2] << 16 |
+             (uint32_t)(uint8_t)q[3] << 24;
+      pk.y = (uint32_t)(uint8_t)q[4] | (uint32_t)(uint8_t)q[5] << 8 | (uint32_t)(uint8_t)q[6] << 16 |
+             (uint32_t)(uint8_t)q[7] << 24;
+      *reinterpret_cast<uint2*>(hq + (int64_t)t * inter + i0) = pk;
+      if ((lane & 3) == 0) hds[((int64_t)t * inter + i0) / Q8B] = make_float2(d, s);
+    }
   }
   frag_token(v, t >= m, t, nt, sb, f);
 }
@@ -584,7 +616,9 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
 }
 
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
-                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16) {
+                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16,
+                          uint8_t* q8h) {
+  const bool q8 = q8h != nullptr;  // activations rounded to Q8_1 (x, and h stored at q8h)
   uint8_t* W = (uint8_t*)ws;
   FragPtrs f1{(uint2*)(W + p.off_fx1), (uint32_t*)(W + p.off_fm1), (float*)(W + p.off_sc1)};
   FragPtrs f2{(uint2*)(W + p.off_fx2), (uint32_t*)(W + p.off_fm2), (float*)(W + p.off_sc2)};
@@ -603,10 +637,14 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
 
   // K0: not a dependent launch, so it also orders this call after the previous one on the stream
   prof.before(0, s);
-  if (bf16)
-    prep_x_kernel<__nv_bfloat16><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
+  if (bf16 && q8)
+    prep_x_kernel<__nv_bfloat16, true><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
+  else if (bf16)
+    prep_x_kernel<__nv_bfloat16, false><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
+  else if (q8)
+    prep_x_kernel<float, true><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
   else
-    prep_x_kernel<float><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
+    prep_x_kernel<float, false><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
   prof.after(0, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -621,9 +659,13 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
     const float* pp = p1;
     int nks = p.nks1, m = p.m, inter = p.inter, nt = p.nt;
     FragPtrs f = f2;
-    void* args[] = {&pp, &nks, &m, &inter, &nt, &f};
+    uint8_t* hq = q8h;
+    float2* hds = q8 ? (float2*)(q8h + (size_t)p.m * p.inter) : nullptr;
+    void* args[] = {&pp, &nks, &m, &inter, &nt, &f, &hq, &hds};
+    const void* fn = q8 ? reinterpret_cast<const void*>(finish_gateup_kernel<true>)
+                        : reinterpret_cast<const void*>(finish_gateup_kernel<false>);
     prof.before(2, s);
-    e = launch_pdl(reinterpret_cast<const void*>(finish_gateup_kernel), dim3(nsb2), dim3(128 * p.nt), 0, s, args);
+    e = launch_pdl(fn, dim3(nsb2), dim3(128 * p.nt), 0, s, args);
     prof.after(2, s);
     if (e != cudaSuccess) return e;
   }

@@ -1,4 +1,8 @@
-// Decode regime (m = 1..8 tokens) with Q8_1 activations, on sm_103a.
+// Decode regime (m = 1..8 tokens) with Q8_1 activations, on sm_103a. One or two
+// tokens run the integer kernels of this file; three to eight run the float32
+// decode path's kernels (decode.cu) on Q8_1-rounded x and h, whose fp16 tensor
+// cores take 4 or 8 token columns at once where the integer epilogue per
+// 32-weight sub-block would dominate.
 //
 //   K0  q8_1(x):           x [m][hidden] -> planar Q8_1 (the stand-alone quantizer's kernel)
 //   K1  gemv_q8<gate/up>:  partial g = Wg.xq and u = Wu.xq per K-chunk, one pass over both
@@ -82,22 +86,10 @@ struct Q8Smem {
   static constexpr size_t BYTES = OFF_FLAG + 16;
 };
 
-// m16n8k32 integer MMA: 4-bit quants as u8 (A), Q8_1 quants as s8 (B), int32 sums.
-__device__ __forceinline__ void mma_u8s8(int c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
-      : "=r"(c[0]), "=r"(c[1]), "=r"(c[2]), "=r"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
-}
-
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
 // COMBOS consecutive tiles of W_down); each warp takes TPW of them at one of the
-// SLICES superblocks. MT >= m tokens. One or two tokens: dp4a, with the
-// activations of the warp's superblock in registers. Three to eight tokens:
-// mma.sync m16n8k32 (u8 weights x s8 activations, the 8 columns are the tokens),
-// one MMA per 32-weight sub-block and 16-row tile; a lane holds its column's
-// (token g's) activation words and the {d8, s8} of its two result columns.
+// SLICES superblocks. MT (1 or 2) >= m tokens, whose activations for the warp's
+// superblock stay in registers; dp4a forms the integer sums.
 template <bool GATEUP, int MT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>
 __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     gemv_q8_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
@@ -207,15 +199,9 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   for (int t = 0; t < TPW; ++t)
 #pragma unroll
     for (int k = 0; k < MT; ++k) acc[t][k][0] = acc[t][k][1] = 0.f;
-  constexpr bool MMA = MT > 2;
-  constexpr int XC = MMA ? 1 : MT;
-  uint4 xa[XC][4];  // dp4a: activation words of sub-block 2 tig (xa[.][0..1]) and 2 tig + 1 (xa[.][2..3])
-  float4 xd[XC];    // dp4a: {d8, s8} of those two blocks
-  uint32_t bx[MMA ? 8 : 1][2];  // MMA: token g's words at positions 4tig.. and 16+4tig.. of sub-block j
-  float2 dx[MMA ? 2 : 1][8];    // MMA: {d8, s8} of tokens 2tig and 2tig+1, sub-block j
-  float accm[MMA ? TPW : 1][2][2];  // MMA: rows g, g+8 x tokens 2tig, 2tig+1
-#pragma unroll
-  for (int t = 0; t < (MMA ? TPW : 1); ++t) accm[t][0][0] = accm[t][0][1] = accm[t][1][0] = accm[t][1][1] = 0.f;
+  static_assert(MT <= 2, "one or two tokens");
+  uint4 xa[MT][4];  // activation words of sub-block 2 tig (xa[.][0..1]) and 2 tig + 1 (xa[.][2..3])
+  float4 xd[MT];    // {d8, s8} of those two blocks
   int csb = -1;
   auto load_x = [&](int tok, int sb, uint4 w[4], float4& d) {
     const int tt = min(tok, P.m - 1);  // padding tokens read a real token; their sums are never stored
@@ -245,75 +231,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     }
     const int sb = cw.g * SLICES + slice;
     const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
-    if constexpr (MMA) {
-      if (!failed && sb < chunk_end) {
-        // ---------------------------------------- TPW 16-row tiles of one superblock, 8 token columns
-        if (sb != csb) {
-          const uint8_t* xp = P.xq + (int64_t)min(g, P.m - 1) * kq + (int64_t)sb * QK + 4 * tig;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            bx[j][0] = *reinterpret_cast<const uint32_t*>(xp + 32 * j);
-            bx[j][1] = *reinterpret_cast<const uint32_t*>(xp + 32 * j + 16);
-          }
-          const float2* ds2 = reinterpret_cast<const float2*>(P.xds);
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int64_t tc = min(2 * tig + c, P.m - 1);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) dx[c][j] = ds2[(tc * P.nsb + sb) * 8 + j];
-          }
-          csb = sb;
-        }
-#pragma unroll
-        for (int t = 0; t < TPW; ++t) {
-          const int cb = tgrp * TPW + t;
-          const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
-                                                                   : (slice * RU + cb * ROWS) * BLK);
-          uint32_t wl[2][4], wh[2][4], sw[2][3];
-          float dd[2], dm[2];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const uint8_t* rb = base + (g + 8 * r) * BLK;
-            const uint4 hd = *reinterpret_cast<const uint4*>(rb);
-            const float2 dpair = __half22float2(u32_as_h2(hd.x));
-            dd[r] = dpair.x;
-            dm[r] = dpair.y;
-#pragma unroll
-            for (int G = 0; G < 4; ++G) {  // quant bytes 4tig.. and 16+4tig.. of group G
-              wl[r][G] = *reinterpret_cast<const uint32_t*>(rb + 16 + 32 * G + 4 * tig);
-              wh[r][G] = *reinterpret_cast<const uint32_t*>(rb + 32 + 32 * G + 4 * tig);
-            }
-            sw[r][0] = hd.y, sw[r][1] = hd.z, sw[r][2] = hd.w;
-          }
-          float sm[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, mn[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t mask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;  // sub-block 2G+1: 16 q in place
-            const int G = j >> 1;
-            int c4[4];
-            mma_u8s8(c4, wl[0][G] & mask, wl[1][G] & mask, wh[0][G] & mask, wh[1][G] & mask, bx[j][0], bx[j][1]);
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              uint32_t sc, mq;
-              scale_min(sw[r][0], sw[r][1], sw[r][2], j, sc, mq);
-              const float mf = __uint_as_float(0x4B000000u | mq) - 8388608.f;
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int v = (j & 1) ? (c4[2 * r + c] >> 4) : c4[2 * r + c];  // exact: the sum is 16 * I
-                // |I * scale| < 2^22: 1.5 * 2^23 + v holds v exactly in its mantissa
-                const float f = __int_as_float(v * (int)sc + 0x4B400000) - 12582912.f;
-                sm[r][c] = fmaf(f, dx[c][j].x, sm[r][c]);
-                mn[r][c] = fmaf(mf, dx[c][j].y, mn[r][c]);
-              }
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int c = 0; c < 2; ++c) accm[t][r][c] = fmaf(dd[r], sm[r][c], fmaf(-dm[r], mn[r][c], accm[t][r][c]));
-        }
-      }
-    } else if (!failed && sb < chunk_end) {
+    if (!failed && sb < chunk_end) {
       // ------------------------------------------ TPW 16-row tiles of one superblock
       uint4 q0[TPW][2], q1[TPW][2];
       int scl[TPW][2], sch[TPW][2];
@@ -344,15 +262,15 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       }
       if (sb != csb) {
 #pragma unroll
-        for (int k = 0; k < XC; ++k) load_x(k, sb, xa[k], xd[k]);
+        for (int k = 0; k < MT; ++k) load_x(k, sb, xa[k], xd[k]);
         csb = sb;
       }
 #pragma unroll
       for (int k = 0; k < MT; ++k) {
         uint4 xw[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xw[i] = xa[MMA ? 0 : k][i];
-        const float4 dsv = xd[MMA ? 0 : k];
+        for (int i = 0; i < 4; ++i) xw[i] = xa[k][i];
+        const float4 dsv = xd[k];
         const uint32_t xl[8] = {xw[0].x, xw[0].y, xw[0].z, xw[0].w, xw[1].x, xw[1].y, xw[1].z, xw[1].w};
         const uint32_t xh[8] = {xw[2].x, xw[2].y, xw[2].z, xw[2].w, xw[3].x, xw[3].y, xw[3].z, xw[3].w};
 #pragma unroll
@@ -384,29 +302,17 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       // the four lanes of a row hold different sub-blocks: sum them; lane tig
       // then writes the tokens congruent to tig mod 4
       float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * PER_WARP + g * TPW * MT * 2;
-      if constexpr (MMA) {
-        // lane tig holds tokens 2tig and 2tig+1 of its rows
 #pragma unroll
-        for (int t = 0; t < TPW; ++t)
+      for (int t = 0; t < TPW; ++t)
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            if (2 * tig + c < MT) {
-              slot[(t * MT + 2 * tig + c) * 2 + 0] = accm[t][0][c];
-              slot[(t * MT + 2 * tig + c) * 2 + 1] = accm[t][1][c];
-            }
-      } else {
+        for (int k = 0; k < MT; ++k)
 #pragma unroll
-        for (int t = 0; t < TPW; ++t)
-#pragma unroll
-          for (int k = 0; k < MT; ++k)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-              float v = acc[t][k][r];
-              v += __shfl_xor_sync(0xffffffffu, v, 1);
-              v += __shfl_xor_sync(0xffffffffu, v, 2);
-              if ((k & 3) == tig) slot[(t * MT + k) * 2 + r] = v;
-            }
-      }
+          for (int r = 0; r < 2; ++r) {
+            float v = acc[t][k][r];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if ((k & 3) == tig) slot[(t * MT + k) * 2 + r] = v;
+          }
       __syncwarp();
       asm volatile("bar.sync 1, %0;" ::"r"(WARPS * 32) : "memory");
       if (warp == 1 + (nunit % (WARPS - 1)) && !*abort_flag) {
@@ -435,8 +341,6 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int k = 0; k < MT; ++k) acc[t][k][0] = acc[t][k][1] = 0.f;
-#pragma unroll
-      for (int t = 0; t < (MMA ? TPW : 1); ++t) accm[t][0][0] = accm[t][0][1] = accm[t][1][0] = accm[t][1][1] = 0.f;
       ++nunit;
       walk_next(cw);
     }
@@ -448,19 +352,16 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   }
 }
 
-// CTA shapes: 8 warps, two CTAs per SM. K1: gate and up boxes, two stages; one or
-// two tokens: two tiles per warp, 8 superblocks per step; three to eight tokens:
-// one tile per warp (fewer registers for the MMA path), 4 superblocks per step. K2, one or two tokens: one tile
-// per warp, boxes of 16 rows x 8 superblocks, three stages, and K left unsplit
-// when the row units fill half the CTA slots (no chunk sum follows); three to
-// eight tokens: two tiles per warp, boxes of 64 rows x 4 superblocks, two stages.
+// CTA shapes: 8 warps, two CTAs per SM. K1: gate and up boxes of 16 rows x 8
+// superblocks, two tiles per warp (gate and up), two stages. K2: one tile per warp,
+// boxes of 16 rows x 8 superblocks, three stages, and K left unsplit when the row
+// units fill half the CTA slots (no chunk sum follows).
 template <bool GATEUP, int MT> struct ShapeQ8;
 template <int MT> struct ShapeQ8<true, MT> {
-  static constexpr int COMBOS = 2, TPW = MT <= 2 ? 2 : 1, SLICES = MT <= 2 ? 8 : 4, STAGES = 2, CPS = 2;
+  static constexpr int COMBOS = 2, TPW = 2, SLICES = 8, STAGES = 2, CPS = 2;
 };
 template <int MT> struct ShapeQ8<false, MT> {
-  static constexpr int COMBOS = MT <= 2 ? 1 : 4, TPW = MT <= 2 ? 1 : 2, SLICES = MT <= 2 ? 8 : 4,
-                       STAGES = MT <= 2 ? 3 : 2, CPS = 2;
+  static constexpr int COMBOS = 1, TPW = 1, SLICES = 8, STAGES = 3, CPS = 2;
 };
 
 template <bool GATEUP, int MT>
@@ -486,12 +387,7 @@ cudaError_t launch_gemv_q8(const CUtensorMap& t0, const CUtensorMap& t1, const G
 template <bool GATEUP>
 cudaError_t launch_gemv_q8_mt(int mt, const CUtensorMap& t0, const CUtensorMap& t1, const GemvQ8Params& P, int grid,
                               cudaStream_t s) {
-  switch (mt) {
-    case 1: return launch_gemv_q8<GATEUP, 1>(t0, t1, P, grid, s);
-    case 2: return launch_gemv_q8<GATEUP, 2>(t0, t1, P, grid, s);
-    case 4: return launch_gemv_q8<GATEUP, 4>(t0, t1, P, grid, s);
-    default: return launch_gemv_q8<GATEUP, 8>(t0, t1, P, grid, s);
-  }
+  return mt == 1 ? launch_gemv_q8<GATEUP, 1>(t0, t1, P, grid, s) : launch_gemv_q8<GATEUP, 2>(t0, t1, P, grid, s);
 }
 
 template <bool GATEUP>
@@ -502,12 +398,10 @@ void shape_q8(int mt, int* combos, int* slices, int* cps) {
     *slices = S::SLICES;
     *cps = S::CPS;
   };
-  switch (mt) {
-    case 1: get(ShapeQ8<GATEUP, 1>{}); break;
-    case 2: get(ShapeQ8<GATEUP, 2>{}); break;
-    case 4: get(ShapeQ8<GATEUP, 4>{}); break;
-    default: get(ShapeQ8<GATEUP, 8>{}); break;
-  }
+  if (mt == 1)
+    get(ShapeQ8<GATEUP, 1>{});
+  else
+    get(ShapeQ8<GATEUP, 2>{});
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -561,23 +455,38 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
   p->hidden = (int)hidden;
   p->inter = (int)inter;
   p->mt = decode_q8_tokens(m);
-  const int nsb1 = (int)(hidden / QK), nsb2 = (int)(inter / QK);
-  int cb1, sl1, cps1, cb2, sl2, cps2;
-  shape_q8<true>(p->mt, &cb1, &sl1, &cps1);
-  shape_q8<false>(p->mt, &cb2, &sl2, &cps2);
-  const int nru1 = (int)(inter / 16), nru2 = (int)(hidden / (16 * cb2));
-  const int max_nks = m <= 4 ? 16 : 8;
-  choose_split((nsb1 + sl1 - 1) / sl1, nru1, num_sms * cps1, max_nks, &p->nks1, &p->kc1);
-  choose_split((nsb2 + sl2 - 1) / sl2, nru2, num_sms * cps2, (p->mt <= 2 && 2 * nru2 >= num_sms * cps2) ? 1 : max_nks,
-               &p->nks2, &p->kc2);
-  p->grid1 = (int)std::min<int64_t>((int64_t)num_sms * cps1, (int64_t)p->nks1 * nru1);
-  p->grid2 = (int)std::min<int64_t>((int64_t)num_sms * cps2, (int64_t)p->nks2 * nru2);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
     o = align256(o + bytes);
     return at;
   };
+  p->fpath = p->mt > 2;
+  if (p->fpath) {
+    // 3-8 tokens: the float32 path's GEMVs (fp16 tensor cores, 4 or 8 token columns) on
+    // Q8_1-rounded x and h beat the integer kernels here, whose every 32-weight
+    // sub-block needs its own scale and min epilogue
+    if (!decode_plan(m, hidden, inter, num_sms, &p->fp)) return false;
+    p->nks1 = p->fp.nks1, p->nks2 = p->fp.nks2;
+    p->off_xq = 0;
+    p->off_hq = take((size_t)m * inter + (size_t)m * (inter / Q8B) * 8);
+    p->off_fp = take(p->fp.ws_bytes);
+    p->off_p1 = p->off_p2 = 0;
+    p->ws_bytes = o;
+    return true;
+  }
+  const int nsb1 = (int)(hidden / QK), nsb2 = (int)(inter / QK);
+  int cb1, sl1, cps1, cb2, sl2, cps2;
+  shape_q8<true>(p->mt, &cb1, &sl1, &cps1);
+  shape_q8<false>(p->mt, &cb2, &sl2, &cps2);
+  const int nru1 = (int)(inter / 16), nru2 = (int)(hidden / (16 * cb2));
+  const int max_nks = 16;
+  choose_split((nsb1 + sl1 - 1) / sl1, nru1, num_sms * cps1, max_nks, &p->nks1, &p->kc1);
+  choose_split((nsb2 + sl2 - 1) / sl2, nru2, num_sms * cps2, 2 * nru2 >= num_sms * cps2 ? 1 : max_nks,
+               &p->nks2, &p->kc2);
+  p->grid1 = (int)std::min<int64_t>((int64_t)num_sms * cps1, (int64_t)p->nks1 * nru1);
+  p->grid2 = (int)std::min<int64_t>((int64_t)num_sms * cps2, (int64_t)p->nks2 * nru2);
+  p->off_fp = 0;
   p->off_xq = take((size_t)m * hidden + (size_t)m * (hidden / Q8B) * 8);
   p->off_hq = take((size_t)m * inter + (size_t)m * (inter / Q8B) * 8);
   p->off_p1 = take((size_t)p->nks1 * 2 * m * inter * 4);
@@ -590,6 +499,7 @@ cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, con
                              const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
                              const ProfileEvents& prof, int ybf16) {
   uint8_t* W = (uint8_t*)ws;
+  if (p.fpath) return launch_decode(p.fp, x, bf16, wg, wu, wd, y, W + p.off_fp, err, s, prof, ybf16, W + p.off_hq);
   uint8_t* xq = W + p.off_xq;
   uint8_t* hq = W + p.off_hq;
   const float4* xds = (const float4*)(xq + (size_t)p.m * p.hidden);

@@ -32,19 +32,24 @@ struct DecodePlan {
 };
 bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p);
 // y is float32, or bf16 when ybf16 (rounded once by the final chunk-sum kernel).
+// With q8h, x and h are rounded to Q8_1 before they become the B operand, and the
+// Q8_1 of h (quants [m][inter], then (d, s) [m][inter/32]) is stored at q8h.
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
-                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16 = 0);
+                          void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16 = 0,
+                          uint8_t* q8h = nullptr);
 
 // ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8 per pass)
 struct DecodeQ8Plan {
   int m, hidden, inter;
   int mt;              // tokens the GEMV kernels are compiled for (1, 2, 4 or 8; >= m)
+  int fpath;           // 3-8 tokens: the float32 path's kernels on Q8_1-rounded activations (fp below)
+  DecodePlan fp;       // that path's plan; its workspace starts at off_fp
   int nks1, kc1;       // gate/up K-chunks and superblock groups per chunk
   int nks2, kc2;       // down K-chunks and superblock groups per chunk
   int grid1, grid2;    // CTAs
   size_t ws_bytes;     // workspace bytes
   // workspace offsets (bytes): planar Q8_1 of x and of h, gate/up and down chunk sums
-  size_t off_xq, off_hq, off_p1, off_p2;
+  size_t off_xq, off_hq, off_p1, off_p2, off_fp;
 };
 int decode_q8_tokens(int64_t m);
 bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodeQ8Plan* p);
