@@ -38,7 +38,7 @@
  *     blocks (row = output feature, blocks run along the input dimension;
  *     realizar q4k_gemv_cached_uses.rs, q4k_gemv_cached: n = output, k = input).
  *   - Regimes: m <= 24 runs the decode path (float32 activations, no
- *     activation quantization) in passes of at most 8 tokens; m >= 25 runs the
+ *     activation quantization) in passes of at most 16 tokens; m >= 25 runs the
  *     prefill path (activations quantized to Q8_1, Q4_K x Q8_1 GEMM on the
  *     tensor cores). ffn_q4k_swiglu_q8_1 quantizes the activations to Q8_1 at
  *     every m (decode passes up to 24 tokens, the prefill path above).
@@ -143,9 +143,11 @@ q4k_status ffn_q4k_swiglu_ex_y(const void* x, q4k_dtype dtype, int64_t m, int64_
  * with exact integer inner sums. Source: realizar src/cuda/executor/layers/
  * ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (the decode pipeline with quantized
  * activations and integer dot products); spark_model/layers/ops/q4k_mmq.rs,
- * q4k_mmq_gemm (the block correction). For m = 1..24 it runs integer-dot GEMVs
- * in passes of at most 8 tokens (x Q8_1, gate+up GEMV, chunk sum + SwiGLU + Q8_1
- * of h, down GEMV, down chunk sum); for m >= 25 it is the same computation as
+ * q4k_mmq_gemm (the block correction). For m = 1..24 it runs decode passes of at
+ * most 16 tokens (x Q8_1, gate+up GEMV, chunk sum + SwiGLU + Q8_1 of h, down GEMV,
+ * down chunk sum); a pass of 1-2 tokens forms integer dot products, one of 3-16
+ * tokens multiplies the dequantized Q8_1 values (q * d) on the fp16 tensor cores
+ * with float32 accumulation; for m >= 25 it is the same computation as
  * ffn_q4k_swiglu_ex's prefill path (and gives the same bytes). x is float32 or bf16 [m][hidden] (bf16 is
  * widened exactly before quantization), y float32 [m][hidden]. The workspace is
  * caller-owned, 256-byte aligned, of at least ffn_q4k_q8_1_workspace_bytes(m,

@@ -80,11 +80,11 @@ q4k_status check_ffn_args(const void* x, int dtype, int64_t m, int64_t hidden, i
 }
 
 // Up to DECODE_MAX tokens the call runs the decode kernels, in passes of at most
-// DECODE_CHUNK tokens (their token tiles hold 8). A pass streams all the weights
-// once; the prefill GEMM at one token tile costs about three passes, so passes
-// win up to 24 tokens on the workloads measured. From 25 tokens on the prefill
-// GEMM runs.
-constexpr int64_t DECODE_CHUNK = 8;
+// DECODE_CHUNK tokens (four token tiles of 4). A pass streams all the weights
+// once: on the LLaMA-7B FFN one 16-token pass takes 56 us and the prefill GEMM
+// at one token tile 122 us, so 24 tokens take 95 us in two passes. From 25 tokens
+// on the prefill GEMM runs (two passes would still win by about 8% up to 32).
+constexpr int64_t DECODE_CHUNK = q4k::DECODE_PASS_MAX;
 constexpr int64_t DECODE_MAX = 24;
 bool is_decode(int64_t m) { return m <= DECODE_MAX; }
 int64_t last_chunk(int64_t m) { return m - DECODE_CHUNK * ((m - 1) / DECODE_CHUNK); }

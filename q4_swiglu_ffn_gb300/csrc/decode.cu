@@ -1,4 +1,4 @@
-// Decode regime (m = 1..8 tokens) of the Q4_K SwiGLU FFN on sm_103a.
+// Decode regime (m = 1..16 tokens per pass) of the Q4_K SwiGLU FFN on sm_103a.
 //
 //   K0  prep_x:         x [m][hidden] -> B fragments (below); per token and superblock
 //   K1  gemv<gate/up>:  partial g = Wg.x and u = Wu.x per K-chunk, one pass over both
@@ -53,7 +53,7 @@ namespace {
 struct FragPtrs {
   uint2* fx;     // [nsb][16 k-steps][nt][32 lanes] main B fragments
   uint32_t* fm;  // [nsb][nt][32 lanes] min-term B fragments (b0b1; b2b3 are zero)
-  float* sc;     // [nsb][8] 2^e per token
+  float* sc;     // [nsb][4 nt] 2^e per token
 };
 
 // One warp turns the 256 inputs of token t of superblock `sb` (this lane holds
@@ -74,7 +74,7 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
       fx[(int64_t)step * nt * 32 + (gbase + 1) * 4] = make_uint2(0u, 0u);
     }
     if ((lane & 7) == 0) fm[gbase * 4] = fm[(gbase + 1) * 4] = 0u;
-    if (lane == 0) f.sc[(int64_t)sb * 8 + t] = 1.f;
+    if (lane == 0) f.sc[(int64_t)sb * 4 * nt + t] = 1.f;
     return;
   }
   float amax = 0.f;
@@ -116,7 +116,7 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
     fm[gbase * 4] = h2_as_u32(__halves2half2(xlh, xhh));
     fm[(gbase + 1) * 4] = h2_as_u32(__halves2half2(xll, xhl));
   }
-  if (lane == 0) f.sc[(int64_t)sb * 8 + t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  if (lane == 0) f.sc[(int64_t)sb * 4 * nt + t] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
 // Loads the 8 inputs of this lane (float32 or bf16, widened exactly).
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           bmc[n] = P.in.fm[((int64_t)sb * NT + n) * 32 + flane[n]];
-          xsc[n] = P.in.sc[(int64_t)sb * 8 + n * 4 + tig];
+          xsc[n] = P.in.sc[(int64_t)sb * 4 * NT + n * 4 + tig];
         }
         csb = sb;
       }
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 // (gate and up of the same rows) sharing the B operand, gate and up boxes of 16
 // rows x 8 superblocks, two stages; K2 one 16-row tile per unit and warp (boxes
 // of 16 rows x 8 superblocks, three stages), which gives enough units to leave K
-// unsplit on large layers, so no chunk sum follows. 5-8 tokens (two token tiles;
+// unsplit on large layers, so no chunk sum follows. 5-16 tokens (two to four token tiles;
 // B read through L1, so that a thread fits in 128 registers): small CTAs, many
 // per SM, which keeps 16 warps per SM without tying them to one CTA barrier per
 // step; K1 4 warps (gate or up tile at 2 superblocks), boxes of 16 rows x 2
@@ -551,6 +551,28 @@ template <> struct Shape<true, 1> { static constexpr int COMBOS = 2, TPW = 2, SL
 template <> struct Shape<false, 1> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 8, STAGES = 3, CPS = 2; };
 template <> struct Shape<true, 2> { static constexpr int COMBOS = 2, TPW = 1, SLICES = 2, STAGES = 2, CPS = 4; };
 template <> struct Shape<false, 2> { static constexpr int COMBOS = 1, TPW = 1, SLICES = 2, STAGES = 3, CPS = 8; };
+template <> struct Shape<true, 3> : Shape<true, 2> {};
+template <> struct Shape<false, 3> : Shape<false, 2> {};
+template <> struct Shape<true, 4> : Shape<true, 2> {};
+template <> struct Shape<false, 4> : Shape<false, 2> {};
+
+struct ShapeVals {
+  int slices, combos, cps;
+};
+template <bool GATEUP, int NT>
+constexpr ShapeVals shape_vals() {
+  return {Shape<GATEUP, NT>::SLICES, Shape<GATEUP, NT>::COMBOS, Shape<GATEUP, NT>::CPS};
+}
+template <bool GATEUP>
+ShapeVals shape_of(int nt) {
+  return nt == 1   ? shape_vals<GATEUP, 1>()
+         : nt == 2 ? shape_vals<GATEUP, 2>()
+         : nt == 3 ? shape_vals<GATEUP, 3>()
+                   : shape_vals<GATEUP, 4>();
+}
+template <bool GATEUP>
+cudaError_t launch_gemv_nt(int nt, const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
+                           cudaStream_t s);
 
 template <bool GATEUP, int NT>
 constexpr size_t gemv_smem() {
@@ -573,25 +595,32 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
                     args);
 }
 
+template <bool GATEUP>
+cudaError_t launch_gemv_nt(int nt, const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
+                           cudaStream_t s) {
+  return nt == 1   ? launch_gemv<GATEUP, 1>(t0, t1, P, grid, s)
+         : nt == 2 ? launch_gemv<GATEUP, 2>(t0, t1, P, grid, s)
+         : nt == 3 ? launch_gemv<GATEUP, 3>(t0, t1, P, grid, s)
+                   : launch_gemv<GATEUP, 4>(t0, t1, P, grid, s);
+}
+
 }  // namespace
 
 bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p) {
-  if (m < 1 || m > 8) return false;
+  if (m < 1 || m > DECODE_PASS_MAX) return false;
   p->m = (int)m;
   p->hidden = (int)hidden;
   p->inter = (int)inter;
   p->nt = (int)((m + 3) / 4);
   const int nsb1 = (int)(hidden / QK), nsb2 = (int)(inter / QK);
   const bool one = p->nt == 1;
-  const int sl1 = one ? Shape<true, 1>::SLICES : Shape<true, 2>::SLICES;
-  const int sl2 = one ? Shape<false, 1>::SLICES : Shape<false, 2>::SLICES;
-  const int cb2 = one ? Shape<false, 1>::COMBOS : Shape<false, 2>::COMBOS;
+  const ShapeVals s1 = shape_of<true>(p->nt), s2 = shape_of<false>(p->nt);
+  const int sl1 = s1.slices, sl2 = s2.slices, cb2 = s2.combos;
   const int nru1 = (int)(inter / 16), nru2 = (int)(hidden / (16 * cb2));
   // at most 16 chunks x 4 tokens of partial sums: with hidden, inter <= 16384 the
   // whole workspace stays under 13.1 MiB
   const int max_nks = 16 / p->nt;
-  const int ctas1 = num_sms * (one ? Shape<true, 1>::CPS : Shape<true, 2>::CPS);
-  const int ctas2 = num_sms * (one ? Shape<false, 1>::CPS : Shape<false, 2>::CPS);
+  const int ctas1 = num_sms * s1.cps, ctas2 = num_sms * s2.cps;
   choose_split((nsb1 + sl1 - 1) / sl1, nru1, ctas1, max_nks, &p->nks1, &p->kc1);
   // K2 leaves K unsplit when its row units alone fill half the CTA slots (no chunk sum to follow)
   choose_split((nsb2 + sl2 - 1) / sl2, nru2, ctas2, (one && 2 * nru2 >= ctas2) ? 1 : max_nks, &p->nks2, &p->kc2);
@@ -605,10 +634,10 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   };
   p->off_fx1 = take((size_t)nsb1 * 16 * p->nt * 32 * 8);
   p->off_fm1 = take((size_t)nsb1 * p->nt * 32 * 4);
-  p->off_sc1 = take((size_t)nsb1 * 8 * 4);
+  p->off_sc1 = take((size_t)nsb1 * 4 * p->nt * 4);
   p->off_fx2 = take((size_t)nsb2 * 16 * p->nt * 32 * 8);
   p->off_fm2 = take((size_t)nsb2 * p->nt * 32 * 4);
-  p->off_sc2 = take((size_t)nsb2 * 8 * 4);
+  p->off_sc2 = take((size_t)nsb2 * 4 * p->nt * 4);
   p->off_p1 = take((size_t)p->nks1 * 2 * m * inter * 4);
   p->off_p2 = take((size_t)p->nks2 * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
@@ -626,10 +655,8 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   const bool k3 = p.nks2 > 1 || ybf16;  // K3 sums the chunks and/or stores bf16
   float* p2 = k3 ? (float*)(W + p.off_p2) : (float*)y;
   const int nsb1 = p.hidden / QK, nsb2 = p.inter / QK;
-  const bool one = p.nt == 1;
-  const int sl1 = one ? Shape<true, 1>::SLICES : Shape<true, 2>::SLICES;
-  const int sl2 = one ? Shape<false, 1>::SLICES : Shape<false, 2>::SLICES;
-  const int cb2 = one ? Shape<false, 1>::COMBOS : Shape<false, 2>::COMBOS;
+  const ShapeVals s1 = shape_of<true>(p.nt), s2 = shape_of<false>(p.nt);
+  const int sl1 = s1.slices, sl2 = s2.slices, cb2 = s2.combos;
   CUtensorMap mg, mu, md;
   if (!weight_map(&mg, wg, p.inter, nsb1, 16, sl1) || !weight_map(&mu, wu, p.inter, nsb1, 16, sl1) ||
       !weight_map(&md, wd, p.hidden, nsb2, 16 * cb2, sl2))
@@ -651,7 +678,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
 
   GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err};
   prof.before(1, s);
-  e = one ? launch_gemv<true, 1>(mg, mu, g1, p.grid1, s) : launch_gemv<true, 2>(mg, mu, g1, p.grid1, s);
+  e = launch_gemv_nt<true>(p.nt, mg, mu, g1, p.grid1, s);
   prof.after(1, s);
   if (e != cudaSuccess) return e;
 
@@ -672,7 +699,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
 
   GemvParams g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, f2, p2, err};
   prof.before(3, s);
-  e = one ? launch_gemv<false, 1>(md, md, g2, p.grid2, s) : launch_gemv<false, 2>(md, md, g2, p.grid2, s);
+  e = launch_gemv_nt<false>(p.nt, md, md, g2, p.grid2, s);
   prof.after(3, s);
   if (e != cudaSuccess) return e;
 

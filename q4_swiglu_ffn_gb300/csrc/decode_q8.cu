@@ -1,7 +1,7 @@
-// Decode regime (m = 1..8 tokens) with Q8_1 activations, on sm_103a. One or two
-// tokens run the integer kernels of this file; three to eight run the float32
+// Decode regime (m = 1..16 tokens per pass) with Q8_1 activations, on sm_103a. One or two
+// tokens run the integer kernels of this file; three to sixteen run the float32
 // decode path's kernels (decode.cu) on Q8_1-rounded x and h, whose fp16 tensor
-// cores take 4 or 8 token columns at once where the integer epilogue per
+// cores take 4 to 16 token columns at once where the integer epilogue per
 // 32-weight sub-block would dominate.
 //
 //   K0  q8_1(x):           x [m][hidden] -> planar Q8_1 (the stand-alone quantizer's kernel)
@@ -450,7 +450,7 @@ __global__ void finish_gateup_q8_kernel(const float* __restrict__ part, int nks,
 int decode_q8_tokens(int64_t m) { return m <= 1 ? 1 : m == 2 ? 2 : m <= 4 ? 4 : 8; }
 
 bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodeQ8Plan* p) {
-  if (m < 1 || m > 8) return false;
+  if (m < 1 || m > DECODE_PASS_MAX) return false;
   p->m = (int)m;
   p->hidden = (int)hidden;
   p->inter = (int)inter;
@@ -463,7 +463,7 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
   };
   p->fpath = p->mt > 2;
   if (p->fpath) {
-    // 3-8 tokens: the float32 path's GEMVs (fp16 tensor cores, 4 or 8 token columns) on
+    // 3-16 tokens: the float32 path's GEMVs (fp16 tensor cores, 4 to 16 token columns) on
     // Q8_1-rounded x and h beat the integer kernels here, whose every 32-weight
     // sub-block needs its own scale and min epilogue
     if (!decode_plan(m, hidden, inter, num_sms, &p->fp)) return false;

@@ -19,10 +19,11 @@ cudaError_t launch_q8_1(const void* x, int bf16, int64_t m, int64_t k, void* out
 cudaError_t launch_quantize_weights(const void* w, int bf16, int64_t rows, int64_t cols, void* out,
                                     uint32_t* err, cudaStream_t s);
 
-// ---------------------------------------------------------------- decode (m <= 8 per pass)
+// ---------------------------------------------------------------- decode (m <= 16 per pass)
+constexpr int DECODE_PASS_MAX = 16;  // tokens of one decode pass
 struct DecodePlan {
   int m, hidden, inter;
-  int nt;              // n-tiles of 4 tokens (1 or 2)
+  int nt;              // n-tiles of 4 tokens (1 to 4)
   int nks1, kc1;       // gate/up K-chunks and superblock groups per chunk
   int nks2, kc2;       // down K-chunks and superblock groups per chunk
   int grid1, grid2;    // CTAs
@@ -38,11 +39,11 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
                           void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16 = 0,
                           uint8_t* q8h = nullptr);
 
-// ---------------------------------------------------------------- decode with Q8_1 activations (m <= 8 per pass)
+// ---------------------------------------------------------------- decode with Q8_1 activations (m <= 16 per pass)
 struct DecodeQ8Plan {
   int m, hidden, inter;
   int mt;              // tokens the GEMV kernels are compiled for (1, 2, 4 or 8; >= m)
-  int fpath;           // 3-8 tokens: the float32 path's kernels on Q8_1-rounded activations (fp below)
+  int fpath;           // 3-16 tokens: the float32 path's kernels on Q8_1-rounded activations (fp below)
   DecodePlan fp;       // that path's plan; its workspace starts at off_fp
   int nks1, kc1;       // gate/up K-chunks and superblock groups per chunk
   int nks2, kc2;       // down K-chunks and superblock groups per chunk

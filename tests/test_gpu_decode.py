@@ -118,17 +118,17 @@ def test_workspace_too_small_is_rejected():
 
 
 @pytest.mark.parametrize("m", [9, 16, 17, 23, 24])
-def test_decode_passes_of_8_tokens(m):
-    """9-24 tokens run as decode passes of at most 8 tokens (float32 activations): each pass's
+def test_decode_passes_of_16_tokens(m):
+    """9-24 tokens run as decode passes of at most 16 tokens (float32 activations): each pass's
     rows equal the call on those tokens alone, and the whole output meets the fp64 oracle."""
     c = workloads.small_config(1024, 1536, m, "f32", ("channels", 0.01, 50.0))
     wg, wu, wd = workloads.weights(c)
     dg, du, dd = to_dev(wg), to_dev(wu), to_dev(wd)
     x, _ = workloads.activations(c)
     y = lib().ffn_q4k_swiglu(to_dev(x), dg, du, dd).cpu().numpy()
-    for t0 in range(0, m, 8):
-        ys = lib().ffn_q4k_swiglu(to_dev(x[t0:t0 + 8]), dg, du, dd).cpu().numpy()
-        assert np.array_equal(y[t0:t0 + 8].view(np.uint32), ys.view(np.uint32))
+    for t0 in range(0, m, 16):
+        ys = lib().ffn_q4k_swiglu(to_dev(x[t0:t0 + 16]), dg, du, dd).cpu().numpy()
+        assert np.array_equal(y[t0:t0 + 16].view(np.uint32), ys.view(np.uint32))
     ref, _ = oracle.ffn_decode(x, wg, wu, wd)
     assert rel_l2(y, ref) <= DECODE_TIGHT
     assert lib().ffn_q4k_workspace_h_q8_1_offset(m, 1024, 1536) == 0

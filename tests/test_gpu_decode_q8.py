@@ -159,8 +159,8 @@ def test_decode_q8_repeated_calls_on_the_same_buffers():
 
 
 @pytest.mark.parametrize("m", [9, 20, 24])
-def test_decode_q8_passes_of_8_tokens(m):
-    """9-24 tokens run as decode passes of at most 8 tokens: each pass's rows equal the call on
+def test_decode_q8_passes_of_16_tokens(m):
+    """9-24 tokens run as decode passes of at most 16 tokens: each pass's rows equal the call on
     those tokens alone, and the whole output meets the Q8_1 oracle."""
     c = workloads.small_config(1024, 1536, m, "f32", ("channels", 0.01, 50.0))
     wg, wu, wd = workloads.weights(c)
@@ -168,11 +168,11 @@ def test_decode_q8_passes_of_8_tokens(m):
     x, _ = workloads.activations(c)
     ws = torch.empty(lib().ffn_q4k_q8_1_workspace_bytes(m, 1024, 1536), dtype=torch.uint8, device=dev())
     y = lib().ffn_q4k_swiglu_q8_1(to_dev(x), dg, du, dd, ws).cpu().numpy()
-    for t0 in range(0, m, 8):
-        xs = x[t0:t0 + 8]
+    for t0 in range(0, m, 16):
+        xs = x[t0:t0 + 16]
         w1 = torch.empty(lib().ffn_q4k_q8_1_workspace_bytes(len(xs), 1024, 1536), dtype=torch.uint8, device=dev())
         ys = lib().ffn_q4k_swiglu_q8_1(to_dev(xs), dg, du, dd, w1).cpu().numpy()
-        assert np.array_equal(y[t0:t0 + 8].view(np.uint32), ys.view(np.uint32))
+        assert np.array_equal(y[t0:t0 + 16].view(np.uint32), ys.view(np.uint32))
     assert rel_l2(y, oracle.ffn_prefill(x, wg, wu, wd)["y"]) <= ACCEPT
     assert lib().ffn_q4k_q8_1_workspace_h_offset(m, 1024, 1536) == 0
 
