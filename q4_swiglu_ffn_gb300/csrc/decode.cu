@@ -50,10 +50,13 @@ namespace q4k {
 
 namespace {
 
+// 2^e entries per superblock: 8 up to two token tiles, 4 per tile beyond
+__host__ __device__ constexpr int sc_stride(int nt) { return nt <= 2 ? 8 : 4 * nt; }
+
 struct FragPtrs {
   uint2* fx;     // [nsb][16 k-steps][nt][32 lanes] main B fragments
   uint32_t* fm;  // [nsb][nt][32 lanes] min-term B fragments (b0b1; b2b3 are zero)
-  float* sc;     // [nsb][4 nt] 2^e per token
+  float* sc;     // [nsb][sc_stride(nt)] 2^e per token
 };
 
 // One warp turns the 256 inputs of token t of superblock `sb` (this lane holds
@@ -74,7 +77,7 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
       fx[(int64_t)step * nt * 32 + (gbase + 1) * 4] = make_uint2(0u, 0u);
     }
     if ((lane & 7) == 0) fm[gbase * 4] = fm[(gbase + 1) * 4] = 0u;
-    if (lane == 0) f.sc[(int64_t)sb * 4 * nt + t] = 1.f;
+    if (lane == 0) f.sc[(int64_t)sb * sc_stride(nt) + t] = 1.f;
     return;
   }
   float amax = 0.f;
@@ -116,7 +119,7 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
     fm[gbase * 4] = h2_as_u32(__halves2half2(xlh, xhh));
     fm[(gbase + 1) * 4] = h2_as_u32(__halves2half2(xll, xhl));
   }
-  if (lane == 0) f.sc[(int64_t)sb * 4 * nt + t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  if (lane == 0) f.sc[(int64_t)sb * sc_stride(nt) + t] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
 // Loads the 8 inputs of this lane (float32 or bf16, widened exactly).
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
           bmc[n] = P.in.fm[((int64_t)sb * NT + n) * 32 + flane[n]];
-          xsc[n] = P.in.sc[(int64_t)sb * 4 * NT + n * 4 + tig];
+          xsc[n] = P.in.sc[(int64_t)sb * sc_stride(NT) + n * 4 + tig];
         }
         csb = sb;
       }
@@ -634,10 +637,10 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   };
   p->off_fx1 = take((size_t)nsb1 * 16 * p->nt * 32 * 8);
   p->off_fm1 = take((size_t)nsb1 * p->nt * 32 * 4);
-  p->off_sc1 = take((size_t)nsb1 * 4 * p->nt * 4);
+  p->off_sc1 = take((size_t)nsb1 * sc_stride(p->nt) * 4);
   p->off_fx2 = take((size_t)nsb2 * 16 * p->nt * 32 * 8);
   p->off_fm2 = take((size_t)nsb2 * p->nt * 32 * 4);
-  p->off_sc2 = take((size_t)nsb2 * 4 * p->nt * 4);
+  p->off_sc2 = take((size_t)nsb2 * sc_stride(p->nt) * 4);
   p->off_p1 = take((size_t)p->nks1 * 2 * m * inter * 4);
   p->off_p2 = take((size_t)p->nks2 * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
