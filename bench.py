@@ -35,8 +35,6 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DECODE_CFG = 1
-PREFILL_CFG = 4
 L2_BYTES = 135_528_448
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -143,7 +141,7 @@ def _cpu_decode_worker(budget_s: float, q):
     import numpy as np
     import oracle
     import workloads
-    cfg = workloads.CONFIGS[DECODE_CFG]
+    cfg = workloads.LLAMA7B_DECODE
     wg, wu, wd = workloads.weights(cfg)
     x, _ = workloads.activations(cfg)
     reps, t_total = 0, 0.0
@@ -179,7 +177,7 @@ def gpu_decode(args, rank, world, dist, path="f32"):
     import workloads
     import q4_swiglu_ffn_gb300 as q
 
-    cfg = workloads.CONFIGS[DECODE_CFG]
+    cfg = workloads.LLAMA7B_DECODE
     dev = torch.device("cuda", torch.cuda.current_device())
     wbytes = cfg.weight_bytes()
     R = max(2, math.ceil(3 * L2_BYTES / wbytes))
@@ -358,7 +356,7 @@ def gpu_prefill(args):
     import workloads
     import q4_swiglu_ffn_gb300 as q
 
-    cfg = workloads.CONFIGS[PREFILL_CFG]
+    cfg = workloads.LONG_PREFILL_27B
     dev = torch.device("cuda", torch.cuda.current_device())
     wg, wu, wd = (torch.from_numpy(a).to(dev) for a in workloads.weights(cfg))
     _, xb = workloads.activations(cfg)
@@ -426,7 +424,7 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     import workloads
-    cfg = workloads.CONFIGS[DECODE_CFG]
+    cfg = workloads.LLAMA7B_DECODE
     metric = "Q4_K SwiGLU FFN: decode weight GB/s vs HBM peak; prefill int8 TOPS vs peak"
     workload = {"workload": cfg.name, "hidden": cfg.hidden, "inter": cfg.inter, "m": cfg.m,
                 "weights": "seeded Q4_K (d, dmin ~ U[0.001, 0.05] fp16, 6-bit scales/mins, 4-bit quants uniform)",

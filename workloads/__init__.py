@@ -181,6 +181,7 @@ CONFIGS = [
     Config(3, "8b-prefill-h4096-i14336-m512", 4096, 14336, 512, "bf16", ("channels", 0.001, 100.0)),
     Config(4, "27b-long-prefill-h5120-i17408-m2048", 5120, 17408, 2048, "bf16", ("entries", 0.0005, 900.0)),
 ]
+TINY_DECODE, LLAMA7B_DECODE, BATCHED_13B_DECODE, PREFILL_8B, LONG_PREFILL_27B = CONFIGS
 
 
 def _choose(seed: int, stream: int, n: int, k: int) -> np.ndarray:
