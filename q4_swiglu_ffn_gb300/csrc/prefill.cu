@@ -149,6 +149,12 @@ struct MmqParams {
   int ksplit;          // slices of K (down only; 1 for gate/up)
   int tiles;           // (row tile, token tile) pairs
   int nwork;           // work items: tiles x ksplit; item w is slice w / tiles of tile w % tiles
+  // Down only, without SPLIT: the tiles from `whole` on (the last, partial round of
+  // items on the SMs) are split along K into tail_q > 1 slices, items whole + j for
+  // j < (tiles - whole) * tail_q (slice j / (tiles - whole) of tile whole + j % (tiles -
+  // whole)), which store partial tiles [tail_q][tiles - whole][TN tokens][TM rows] in tail
+  int whole, tail_q;
+  float* tail;
   int mt_fast;         // consecutive CTAs take consecutive row tiles (else consecutive token tiles)
   const float* tscale; // 2^e_t per token
   int8_t* hq_qs;       // gate/up: Q8_1 quants of h [m][inter]
@@ -239,15 +245,24 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   const int64_t rowbytes = (int64_t)P.nsb * BLK;
   struct Work {
     int nt, mt, ks, sb0, nsbl;  // token tile, row tile, K slice, its superblocks [sb0, sb0 + nsbl)
+    int tl;                     // index among the split tail tiles, or -1
   };
   auto work = [&](int w) {
     Work k;
+    k.tl = -1;
     k.ks = SPLIT ? w / P.tiles : 0;
-    const int tile = w - k.ks * P.tiles;
+    int tile = w - k.ks * P.tiles;
+    if (!SPLIT && !GATEUP && P.tail_q > 1 && w >= P.whole) {
+      const int j = w - P.whole, ntail = P.tiles - P.whole;
+      k.tl = j % ntail;
+      k.ks = j / ntail;
+      tile = P.whole + k.tl;
+    }
     k.nt = P.mt_fast ? tile / nmt : tile % P.ntn;
     k.mt = P.mt_fast ? tile % nmt : tile / P.ntn;
-    k.sb0 = SPLIT ? (int)((int64_t)P.nsb * k.ks / P.ksplit) : 0;
-    k.nsbl = SPLIT ? (int)((int64_t)P.nsb * (k.ks + 1) / P.ksplit) - k.sb0 : P.nsb;
+    const int nsl = SPLIT ? P.ksplit : k.tl >= 0 ? P.tail_q : 1;  // K slices of this item's tile
+    k.sb0 = (int)((int64_t)P.nsb * k.ks / nsl);
+    k.nsbl = (int)((int64_t)P.nsb * (k.ks + 1) / nsl) - k.sb0;
     return k;
   };
   // the Q4_K row of tile row r (0-63 gate, 64-127 up for gate/up), at the item's first superblock
@@ -473,6 +488,14 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         __syncwarp();
         asm volatile("bar.sync 2, 256;" ::: "memory");
         gateup_final(xg, P, k.mt, k.nt, warp - W_EPI, lane, abort_flag);
+      } else if (ok && k.tl >= 0) {
+        // a slice of a split tail tile: its partial tile, token-major, rows contiguous
+        float* so = P.tail + ((int64_t)k.ks * (P.tiles - P.whole) + k.tl) * TM * TN;
+#pragma unroll
+        for (int i = 0; i < TN / 2; ++i) {
+          const int t = t0 + c0 + i;
+          so[(int64_t)(c0 + i) * TM + r] = t < P.m ? acc[i] * P.tscale[t] : 0.f;
+        }
       } else if (ok) {
         const int row = k.mt * TM + r;
         float* yo = P.y + (int64_t)k.ks * P.m * P.ldo;
@@ -499,6 +522,35 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
   }
+}
+
+// The split tail tiles of the down projection: y = the sum of the tail_q partial tiles,
+// in slice order. One CTA per (tail tile, 8 tokens), a thread per row.
+__global__ void __launch_bounds__(TM) finish_tail_kernel(const float* __restrict__ tail, int whole, int tiles,
+                                                         int tail_q, int ntn, int mt_fast, int m, int ldo,
+                                                         float* __restrict__ y) {
+  pdl_wait();
+  const int ntail = tiles - whole, tl = blockIdx.x % ntail, t8 = blockIdx.x / ntail;
+  const int tile = whole + tl, nmt = tiles / ntn;
+  const int nt = mt_fast ? tile / nmt : tile % ntn, mt = mt_fast ? tile % nmt : tile / ntn;
+  const int r = threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int tt = t8 * 8 + i, t = nt * TN + tt;
+    if (t >= m) break;
+    float v = 0.f;
+    for (int q = 0; q < tail_q; ++q) v += tail[(((int64_t)q * ntail + tl) * TN + tt) * TM + r];
+    y[(int64_t)t * ldo + mt * TM + r] = v;
+  }
+}
+
+// Split of the down projection's last, partial round of tiles over num_sms persistent
+// CTAs: whole tiles before `whole`, the rest in q > 1 K slices each (q = 0 when the tiles
+// make whole rounds, fit one round, or leave too many for two slices each).
+void tail_split(int tiles, int num_sms, int* whole, int* q) {
+  const int rounds = tiles / num_sms, ntail = tiles - rounds * num_sms;
+  *whole = rounds * num_sms;
+  *q = (rounds > 0 && ntail > 0 && num_sms / ntail >= 2) ? std::min(num_sms / ntail, 8) : 0;
 }
 
 // ------------------------------------------------------------------------- host side
@@ -583,6 +635,10 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   p->off_misc = take(256);
   p->ksplit = down_ksplit(m, hidden, inter, num_sms);
   p->num_sms = num_sms;
+  const int dtiles = (int)((hidden / TM) * ((m + TN - 1) / TN));
+  p->tail_whole = dtiles, p->tail_q = 0;
+  if (p->ksplit == 1) tail_split(dtiles, num_sms, &p->tail_whole, &p->tail_q);
+  p->off_tail = take(p->tail_q > 1 ? (size_t)(dtiles - p->tail_whole) * p->tail_q * TM * TN * 4 : 0);
   p->off_ypart = take((size_t)p->ksplit * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
@@ -662,6 +718,10 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.mt_fast = row_tiles_fastest(H / TM, ntn, I, p.num_sms);
   dn.tiles = (int)(H / TM) * ntn;
   dn.nwork = dn.tiles * p.ksplit;
+  dn.whole = p.tail_whole;
+  dn.tail_q = p.tail_q;
+  dn.tail = (float*)(W + p.off_tail);
+  if (p.tail_q > 1) dn.nwork = p.tail_whole + (dn.tiles - p.tail_whole) * p.tail_q;
   dn.tscale = ho.scale;
   float* ypart = (float*)(W + p.off_ypart);
   const bool fin = p.ksplit > 1 || ybf16;  // the slice sum and/or the bf16 store
@@ -670,6 +730,12 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   prof.before(4, s);  // the down MMQ, and the sum of its K slices when there are several
   e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s)
                    : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s);
+  if (e == cudaSuccess && p.tail_q > 1) {
+    const int ntail = dn.tiles - p.tail_whole;
+    finish_tail_kernel<<<ntail * (TN / 8), TM, 0, s>>>(dn.tail, p.tail_whole, dn.tiles, p.tail_q, ntn, dn.mt_fast,
+                                                     (int)m, (int)H, dn.y);
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess && fin) e = launch_finish_down(ypart, p.ksplit, m * H, y, ybf16, s);
   prof.after(4, s);
   return e;
