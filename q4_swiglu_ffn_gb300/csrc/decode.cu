@@ -27,17 +27,18 @@
 // mins and whose B holds X_j * 2^-(e+6) split into hi and lo.
 //
 // Streaming. A CTA walks a contiguous range of units; a unit is a set of
-// 16-row tiles (gate and up of one tile in K1, four consecutive tiles of
+// 16-row tiles (gate and up of one tile in K1, COMBOS consecutive tiles of
 // W_down in K2) over one K-chunk. Each step loads, with one 3-D TMA box per
 // matrix, the next group of SLICES consecutive superblocks of those rows
-// (1152 or 576 contiguous bytes per row) into a stage of a ring shared by the
+// (SLICES x 144 contiguous bytes per row) into a stage of a ring shared by the
 // CTA; in shared memory the box is laid out
 // superblock-major, 144 bytes per row, so the fragment loads are free of bank
 // conflicts. Each warp takes TPW of the unit's tiles at one superblock of the
-// group and keeps that superblock's B fragments in registers while it stays the
-// same. At the end of a unit an owner warp (rotating) sums the SLICES partial
-// dot products through shared memory and stores them; the chunks are summed by
-// K1b / K3 in a fixed order, so results are deterministic.
+// group; with one token tile it keeps that superblock's B fragments in
+// registers while it stays the same. At the end of a unit an owner warp
+// (rotating) sums the SLICES partial dot products through shared memory and
+// stores them; the chunks are summed by K1b / K3 in a fixed order, so results
+// are deterministic.
 #include <algorithm>
 #include <cmath>
 

@@ -6,8 +6,12 @@
 //                          h = silu(G) * U, h -> planar Q8_1 (hq)
 //   P3 expand(hq)
 //   P4 mmq<down>           y = deq(Wd) . deq(hq), float32 (at small m split into K slices
-//                          that fill one wave, each writing partial sums)
+//                          that fill one wave, each writing partial sums; at large m
+//                          only the last, partial round of tiles is split)
+//   P4b finish_tail        the split tail tiles' sum, in slice order (only then)
 //   P5 finish_down         the slices' sum in slice order, and/or y stored as bf16 (only then)
+// Both MMQ kernels are persistent: one CTA per SM walks the (row tile, token tile)
+// items with its pipelines running on across items.
 // Source: spark_model/layers/ops/q4k_mmq.rs (per-prefill activations to Q8_1,
 // then the Q4_K MMQ GEMM C[m, n] = A_q8[m, k] x W_q4k[n, k]); realizar
 // layers/ffn.rs, fused_ffn_swiglu_gpu_true_dp4a (x quantized to Q8_1 once for
