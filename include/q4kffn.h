@@ -174,14 +174,17 @@ size_t ffn_q4k_q8_1_workspace_h_offset(int64_t m, int64_t hidden, int64_t inter)
  * library image (a file-scope __device__ array that every GPU loading the
  * library holds until the process exits), enough for every accepted shape; m
  * outside 1..8 or a dimension above 16384 returns Q4K_ERR_SHAPE, and a shape
- * whose scratch would still exceed 16 MiB (possible only on parts with other SM
- * counts) returns Q4K_ERR_NOMEM, both without launching. The first call on a device resolves the
- * array's device address (cudaGetSymbolAddress) and checks the architecture,
- * so make that first call before any stream capture. Every call on a device
- * shares the one array and each call re-initialises what it reads; calls that
- * overlap on the GPU (different streams, no ordering) race on it and must not
- * be issued. Device-side wait timeouts of this entry point are recorded in a
- * separate static word that q4k_check_device_error does not read. */
+ * whose scratch would still exceed 16 MiB returns Q4K_ERR_NOMEM, both without
+ * launching. x and y follow the other FFN entry points: device memory, or
+ * mapped page-locked host memory (anything else returns Q4K_ERR_MEMORY before
+ * launch). The first call on a device checks the architecture and resolves
+ * the array's device address (cudaGetSymbolAddress), so make that first call
+ * before any stream capture. Every call on a device shares the one array and
+ * each call re-initialises what it reads; calls that overlap on the GPU
+ * (different streams, no ordering) race on it and must not be issued. Device
+ * wait timeouts are recorded in the library's error word (q4k_check_device_error);
+ * failed calls set q4k_get_last_error and successful ones q4k_last_call_kernels,
+ * as for the other entry points. */
 q4k_status ffn_q4k_swiglu_noalloc(const void* x, int64_t m, int64_t hidden, int64_t inter,
                                   const void* W_gate, const void* W_up, const void* W_down,
                                   float* y, q4k_stream_t stream);

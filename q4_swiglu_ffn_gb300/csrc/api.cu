@@ -11,11 +11,18 @@
 #include <cstring>
 #include <mutex>
 
+#include "api_internal.h"
 #include "common.cuh"
 #include "kernels.h"
 #include "q4kffn.h"
 
 namespace {
+
+// The device error word: a file-scope __device__ word, so that no entry point
+// has to allocate device memory for it (every GPU that loads the library holds
+// its own copy, zero at load). Host code turns its name into this device's
+// address with cudaGetSymbolAddress once per device.
+__device__ uint32_t g_error_word;
 
 thread_local q4k_status g_last = Q4K_OK;
 thread_local q4k::ProfileEvents g_prof;
@@ -34,7 +41,7 @@ struct DeviceState {
   bool checked = false;
   bool ok = false;
   int sms = 0;
-  uint32_t* err = nullptr;  // device error word
+  uint32_t* err = nullptr;  // device address of g_error_word on this device
   void* ws = nullptr;       // default workspace of ffn_q4k_swiglu
   size_t ws_bytes = 0;
   std::mutex mu;
@@ -54,9 +61,9 @@ q4k_status device_state(DeviceState** out) {
         cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return Q4K_ERR_CUDA;
     d.ok = (major == 10 && minor == 3);
-    if (d.ok) {
-      if (cudaMalloc(&d.err, sizeof(uint32_t)) != cudaSuccess) return Q4K_ERR_NOMEM;
-      if (cudaMemset(d.err, 0, sizeof(uint32_t)) != cudaSuccess) return Q4K_ERR_CUDA;
+    if (d.ok && cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return Q4K_ERR_CUDA;
     }
     d.checked = true;
   }
@@ -284,6 +291,25 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
 }
 
 }  // namespace
+
+namespace q4k {
+
+q4k_status current_device(int* sms, uint32_t** err) {
+  DeviceState* d = nullptr;
+  const q4k_status st = device_state(&d);
+  if (st != Q4K_OK) return st;
+  *sms = d->sms;
+  *err = d->err;
+  return Q4K_OK;
+}
+
+q4k_status resolve_host_io(const void** x, float** y) { return resolve_xy(x, y); }
+
+q4k_status record_failure(q4k_status s) { return fail(s); }
+
+void record_kernels(int n) { g_kernels = n; }
+
+}  // namespace q4k
 
 extern "C" {
 

@@ -21,6 +21,12 @@ cudaError_t launch_quantize_weights(const void* w, int bf16, int64_t rows, int64
 
 // ---------------------------------------------------------------- decode (m <= 16 per pass)
 constexpr int DECODE_PASS_MAX = 16;  // tokens of one decode pass
+
+// The allocation-free decode entry point: its static scratch array and the
+// largest shapes it accepts (every such shape's plan fits in the array).
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(16) << 20;
+constexpr int NOALLOC_MAX_TOKENS = 8;
+constexpr int NOALLOC_MAX_DIM = 16384;
 struct DecodePlan {
   int m, hidden, inter;
   int nt;              // n-tiles of 4 tokens (1 to 4)

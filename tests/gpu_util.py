@@ -40,3 +40,35 @@ def rel_l2(y, ref) -> float:
     y = np.asarray(y, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     return float(np.linalg.norm(y - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def rel_max(y, ref) -> float:
+    """Element-wise error: max |y - ref| over max |ref| (both over the whole output)."""
+    y = np.asarray(y, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return float(np.max(np.abs(y - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+# Tolerances. Acceptance for the FFN output: L2-relative error <= 1e-3, and
+# every element within 1e-3 of the output's largest magnitude. Paths whose
+# arithmetic sits far below that (float32 activations carried as fp16 hi + lo,
+# about 22 bits, exact weights, float32 sums) also meet TIGHT_L2 / TIGHT_MAX,
+# which a dropped term or a wrong index could not.
+ACCEPT_L2, ACCEPT_MAX = 1e-3, 1e-3
+TIGHT_L2, TIGHT_MAX = 2e-5, 1e-4
+
+_REPORT = []  # (test id, what, rel_l2, rel_max), printed by the session summary
+
+
+def check_close(y, ref, l2, elem, what="y"):
+    """Asserts rel_l2(y, ref) <= l2 and rel_max(y, ref) <= elem, and records both."""
+    import os
+    e2, em = rel_l2(y, ref), rel_max(y, ref)
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    _REPORT.append((test, what, e2, em))
+    assert e2 <= l2 and em <= elem, f"{what}: rel_l2 {e2:.3g} (bound {l2:g}), rel_max {em:.3g} (bound {elem:g})"
+    return e2, em
+
+
+def report_lines():
+    return [f"{t}  {w}: rel_l2 {a:.3e}  rel_max {b:.3e}" for (t, w, a, b) in _REPORT]

@@ -45,6 +45,15 @@ void check_decode(int sms) {
         CHECK(p.off_p1 + (size_t)p.nks1 * 2 * m * i * 4 <= p.off_p2, "m %d h %d i %d gate/up sums", m, h, i);
         CHECK(p.off_p2 + (size_t)p.nks2 * m * h * 4 <= p.ws_bytes, "m %d h %d i %d down sums", m, h, i);
       }
+  // the allocation-free entry point's static scratch holds every shape it accepts
+  for (int m = 1; m <= q4k::NOALLOC_MAX_TOKENS; ++m)
+    for (int h : kDims)
+      for (int i : kDims) {
+        if (h > q4k::NOALLOC_MAX_DIM || i > q4k::NOALLOC_MAX_DIM) continue;
+        q4k::DecodePlan p;
+        CHECK(q4k::decode_plan(m, h, i, sms, &p) && p.ws_bytes <= q4k::NOALLOC_SCRATCH_BYTES,
+              "noalloc m %d h %d i %d: %zu bytes", m, h, i, p.ws_bytes);
+      }
   q4k::DecodePlan p;
   CHECK(!q4k::decode_plan(0, 4096, 11008, sms, &p), "m 0");
   CHECK(!q4k::decode_plan(q4k::DECODE_PASS_MAX + 1, 4096, 11008, sms, &p), "m above a pass");
@@ -117,7 +126,7 @@ void check_q6k(int sms) {
 }  // namespace
 
 int main() {
-  for (int sms : {152, 148, 132}) {
+  for (int sms : {152, 148, 132, 160, 170}) {
     check_decode(sms);
     check_decode_q8(sms);
     check_prefill(sms);

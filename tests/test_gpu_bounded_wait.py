@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import workloads
-from tests.gpu_util import lib, rel_l2, to_dev, torch
+from tests.gpu_util import TIGHT_L2, TIGHT_MAX, check_close, lib, to_dev, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -45,5 +45,5 @@ def test_context_usable_after_a_timeout():
     y = q.ffn_q4k_swiglu(to_dev(x), to_dev(wg), to_dev(wu), to_dev(wd))
     torch.cuda.synchronize()
     ref, _ = oracle.ffn_decode(x, wg, wu, wd)
-    assert rel_l2(y.cpu().numpy(), ref) < 2e-5
+    check_close(y.cpu().numpy(), ref, TIGHT_L2, TIGHT_MAX)
     assert q.q4k_check_device_error() == Q4K_OK

@@ -4,15 +4,14 @@ import pytest
 
 import oracle
 import workloads
-from tests.gpu_util import dev, guarded_f32, guards_intact, lib, rel_l2, to_dev, torch
+from tests.gpu_util import TIGHT_L2, TIGHT_MAX, check_close, dev, guarded_f32, guards_intact, lib, to_dev, torch
 
 pytestmark = pytest.mark.gpu
 
-# Acceptance bound (BASELINE): L2-relative error <= 1e-3. The decode arithmetic
-# (fp16 hi+lo activations, ~2^-22 relative, exact q*scale, fp32 accumulation)
-# sits far below it; DECODE_TIGHT catches a slip the acceptance bound would hide.
-ACCEPT = 1e-3
-DECODE_TIGHT = 2e-5
+# The acceptance bounds are 1e-3 (L2-relative and element-wise). The decode
+# arithmetic (fp16 hi+lo activations, ~2^-22 relative, exact q*scale, fp32
+# accumulation) sits far below them; the TIGHT bounds catch a slip the
+# acceptance bounds would hide.
 
 
 def _run(cfg, x=None, m=None):
@@ -31,8 +30,7 @@ def _run(cfg, x=None, m=None):
 @pytest.mark.parametrize("cfg_index", [0, 1, 2])
 def test_decode_workloads(cfg_index):
     y, ref = _run(workloads.CONFIGS[cfg_index])
-    err = rel_l2(y, ref)
-    assert err <= ACCEPT and err <= DECODE_TIGHT, err
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX, f"config {cfg_index}")
     assert lib().q4k_check_device_error() == 0
 
 
@@ -42,8 +40,7 @@ def test_decode_workloads(cfg_index):
 def test_decode_shape_sweep(H, I, m):
     c = workloads.small_config(H, I, m, "f32", ("channels", 0.01, 50.0))
     y, ref = _run(c)
-    err = rel_l2(y, ref)
-    assert err <= DECODE_TIGHT, err
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX)
 
 
 def test_decode_repeatable_and_deterministic():
@@ -71,7 +68,7 @@ def test_decode_repeated_calls_on_the_same_buffers():
         lib().ffn_q4k_swiglu(xd, dg, du, dd, y=y)
         torch.cuda.synchronize()
         ref, _ = oracle.ffn_decode(x, wg, wu, wd)
-        assert rel_l2(y.cpu().numpy(), ref) <= DECODE_TIGHT, k
+        check_close(y.cpu().numpy(), ref, TIGHT_L2, TIGHT_MAX, f"call {k}")
         outs.append(y.cpu().numpy().copy())
     x, _ = workloads.activations(c, seed=c.seed)  # the first input again: the same bits
     xd.copy_(torch.from_numpy(x))
@@ -93,7 +90,7 @@ def test_decode_special_inputs():
     x[1] = workloads.normal(5, 2, 512) * 1e-6
     x[2, ::7] = 3.0e5
     y, ref = _run(c, x=x)
-    assert rel_l2(y, ref) <= DECODE_TIGHT
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX)
 
 
 def test_decode_bf16_input_through_ex():
@@ -103,7 +100,7 @@ def test_decode_bf16_input_through_ex():
     ws = torch.zeros(lib().ffn_q4k_workspace_bytes(4, 768, 1024), dtype=torch.uint8, device=dev())
     y = lib().ffn_q4k_swiglu_ex(to_dev(xb), to_dev(wg), to_dev(wu), to_dev(wd), ws)
     ref, _ = oracle.ffn_decode(xf, wg, wu, wd)
-    assert rel_l2(y.cpu().numpy(), ref) <= DECODE_TIGHT
+    check_close(y.cpu().numpy(), ref, TIGHT_L2, TIGHT_MAX)
 
 
 def test_workspace_too_small_is_rejected():
@@ -130,5 +127,5 @@ def test_decode_passes_of_16_tokens(m):
         ys = lib().ffn_q4k_swiglu(to_dev(x[t0:t0 + 16]), dg, du, dd).cpu().numpy()
         assert np.array_equal(y[t0:t0 + 16].view(np.uint32), ys.view(np.uint32))
     ref, _ = oracle.ffn_decode(x, wg, wu, wd)
-    assert rel_l2(y, ref) <= DECODE_TIGHT
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX)
     assert lib().ffn_q4k_workspace_h_q8_1_offset(m, 1024, 1536) == 0

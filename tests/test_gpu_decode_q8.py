@@ -11,12 +11,12 @@ import pytest
 
 import oracle
 import workloads
-from tests.gpu_util import dev, guarded_f32, guards_intact, lib, rel_l2, to_dev, torch
+from tests.gpu_util import (ACCEPT_L2, ACCEPT_MAX, TIGHT_MAX, check_close, dev, guarded_f32, guards_intact, lib,
+                            to_dev, torch)
 
 pytestmark = pytest.mark.gpu
 
-ACCEPT = 1e-3          # acceptance bound: L2-relative error of y against the oracle
-DOWN_TIGHT = 1e-5      # y against the oracle's down stage fed the GPU's own Q8_1(h)
+DOWN_TIGHT = 1e-5      # y against the oracle's down stage fed the GPU's own Q8_1(h), L2-relative
 HQ_FLIP_FRAC = 2e-3    # Q8_1(h) bytes may differ where h sits on a rounding boundary
 HQ_FAR_FRAC = 1e-4     # ... or, rarely, by more than one step where g or u nearly cancels
 
@@ -44,8 +44,7 @@ def _run(cfg, x=None, m=None, bf16=False):
 
 
 def _check(y, ref, hq_gpu, wd):
-    err = rel_l2(y, ref["y"])
-    assert err <= ACCEPT, err
+    err, _ = check_close(y, ref["y"], ACCEPT_L2, ACCEPT_MAX)
     hq, hd, _ = ref["hq"]
     gq, gd, gs = hq_gpu
     flips = np.count_nonzero(gq != hq)
@@ -58,7 +57,7 @@ def _check(y, ref, hq_gpu, wd):
     sums = gq.reshape(gq.shape[0], -1, 32).astype(np.int64).sum(axis=2).astype(np.float32)
     assert np.array_equal(gs, (gd * sums).astype(np.float32))
     # the down GEMV alone, fed the GPU's own Q8_1(h)
-    assert rel_l2(y, oracle.ffn_down_from_q8_1(gq, gd, wd)) <= DOWN_TIGHT
+    check_close(y, oracle.ffn_down_from_q8_1(gq, gd, wd), DOWN_TIGHT, TIGHT_MAX, "down stage on the GPU's Q8_1(h)")
     return err
 
 
@@ -131,8 +130,8 @@ def test_decode_q8_one_hot_weights():
     assert np.count_nonzero(gq != hq) <= 2
     assert np.all(np.abs(gq.astype(int) - hq.astype(int)) <= 1)
     # down: a gather of the GPU's own Q8_1(h), exact up to the float32 product d8 * q8
-    assert rel_l2(y, oracle.dequantize_q8_1(gq, gd)[:, sd]) <= 1e-6
-    assert rel_l2(y, y_hand) <= ACCEPT
+    check_close(y, oracle.dequantize_q8_1(gq, gd)[:, sd], 1e-6, 1e-6, "gather of the GPU's Q8_1(h)")
+    check_close(y, y_hand, ACCEPT_L2, ACCEPT_MAX, "hand-computed gather")
 
 
 def test_decode_q8_repeated_calls_on_the_same_buffers():
@@ -149,7 +148,7 @@ def test_decode_q8_repeated_calls_on_the_same_buffers():
         xd.copy_(torch.from_numpy(x))
         lib().ffn_q4k_swiglu_q8_1(xd, dg, du, dd, ws, y=y)
         torch.cuda.synchronize()
-        assert rel_l2(y.cpu().numpy(), oracle.ffn_prefill(x, wg, wu, wd)["y"]) <= ACCEPT, k
+        check_close(y.cpu().numpy(), oracle.ffn_prefill(x, wg, wu, wd)["y"], ACCEPT_L2, ACCEPT_MAX, f"call {k}")
         outs.append(y.cpu().numpy().copy())
     x, _ = workloads.activations(c, seed=c.seed)
     xd.copy_(torch.from_numpy(x))
@@ -173,7 +172,7 @@ def test_decode_q8_passes_of_16_tokens(m):
         w1 = torch.empty(lib().ffn_q4k_q8_1_workspace_bytes(len(xs), 1024, 1536), dtype=torch.uint8, device=dev())
         ys = lib().ffn_q4k_swiglu_q8_1(to_dev(xs), dg, du, dd, w1).cpu().numpy()
         assert np.array_equal(y[t0:t0 + 16].view(np.uint32), ys.view(np.uint32))
-    assert rel_l2(y, oracle.ffn_prefill(x, wg, wu, wd)["y"]) <= ACCEPT
+    check_close(y, oracle.ffn_prefill(x, wg, wu, wd)["y"], ACCEPT_L2, ACCEPT_MAX)
     assert lib().ffn_q4k_q8_1_workspace_h_offset(m, 1024, 1536) == 0
 
 

@@ -4,12 +4,11 @@ import pytest
 
 import oracle
 import workloads
-from tests.gpu_util import dev, guarded_f32, guards_intact, lib, rel_l2, to_dev, torch
+from tests.gpu_util import TIGHT_L2, TIGHT_MAX, check_close, dev, guarded_f32, guards_intact, lib, to_dev, torch
 
 pytestmark = pytest.mark.gpu
 
-ACCEPT = 1e-3   # acceptance bound: L2-relative error of y against the fp64 oracle
-TIGHT = 2e-5    # x carried as fp16 hi + lo (about 22 bits), exact weights, fp32 sums
+# x carried as fp16 hi + lo (about 22 bits), exact weights, fp32 sums: the TIGHT bounds
 
 
 def _gemv(x_in, blocks, m, n, k):
@@ -36,7 +35,7 @@ def test_q6k_lmhead_tiny():
     c = workloads.LMHEADS[0]
     blocks, x = workloads.lmhead_weights(c), workloads.lmhead_x(c)
     y = _gemv(x, blocks, c.m, c.n, c.k)
-    assert rel_l2(y, oracle.gemv_q6k(x, blocks)) <= TIGHT
+    check_close(y, oracle.gemv_q6k(x, blocks), TIGHT_L2, TIGHT_MAX)
 
 
 def test_q6k_lmhead_llama7b_sampled_rows():
@@ -47,7 +46,7 @@ def test_q6k_lmhead_llama7b_sampled_rows():
     rng = np.random.default_rng(6)
     rows = np.sort(np.concatenate([[0, 15, 16, c.n - 1], rng.choice(c.n, 636, replace=False)]))
     ref = oracle.gemv_q6k(x, blocks[rows])
-    assert rel_l2(y[:, rows], ref) <= TIGHT
+    check_close(y[:, rows], ref, TIGHT_L2, TIGHT_MAX)
     assert np.isfinite(y).all()
 
 
@@ -60,7 +59,7 @@ def test_q6k_shape_sweep(m, n, k):
     x = workloads.normal(31 + m, 4, m * k).reshape(m, k).astype(np.float32)
     x[:, :: max(1, k // 7)] *= 40.0   # a few large channels
     y = _gemv(x, blocks, m, n, k)
-    assert rel_l2(y, oracle.gemv_q6k(x, blocks)) <= TIGHT
+    check_close(y, oracle.gemv_q6k(x, blocks), TIGHT_L2, TIGHT_MAX)
 
 
 def test_q6k_bf16_input_one_hot_is_exact():

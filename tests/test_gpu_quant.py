@@ -4,6 +4,7 @@ import pytest
 
 import oracle
 import workloads
+from tests.golden_files import q8_1_blocks, q8_1_byte_vector
 from tests.gpu_util import dev, lib, to_dev, torch
 
 pytestmark = pytest.mark.gpu
@@ -72,6 +73,35 @@ def test_q8_1_ties_zero_and_single_blocks():
     # the same values through the bf16 path (values chosen exactly representable where it matters)
     bits = workloads.f32_to_bf16_bits(x)
     _q8_check(workloads.bf16_bits_to_f32(bits).reshape(3, 256), bits.reshape(3, 256), 3, 256)
+
+
+def test_q8_1_hand_written_bytes():
+    """The GPU quantizer's bytes equal the vector written out by hand (layout and values)."""
+    x, want = q8_1_byte_vector()
+    out = torch.empty(want.size, dtype=torch.uint8, device=dev())
+    lib().q8_1_quantize_act(to_dev(x), out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got, want), f"first mismatch at byte {int(np.argmax(got != want))}"
+
+
+def test_q8_1_hand_worked_blocks():
+    """Hand-worked blocks, including amax exactly 2^-120 (subnormal d) and the float32 below it."""
+    blocks = list(q8_1_blocks().values())
+    x = np.stack([b["x"] for b in blocks]).reshape(1, -1)
+    x = np.concatenate([x, np.zeros((1, (-x.shape[1]) % 256), np.float32)], axis=1)
+    k = x.shape[1]
+    out = torch.empty(lib().q8_1_bytes(1, k), dtype=torch.uint8, device=dev())
+    lib().q8_1_quantize_act(to_dev(x), out)
+    torch.cuda.synchronize()
+    q, d, s = oracle.q8_1_from_bytes(out.cpu().numpy(), 1, k)
+    for i, b in enumerate(blocks):
+        assert np.array_equal(q[0, 32 * i:32 * i + 32].astype(np.int64), b["q"]), i
+        if "d" in b:
+            assert d[0, i] == np.float32(b["d"]) and s[0, i] == np.float32(b["s"]), i
+        if "dbits" in b:
+            assert int(d[0, i:i + 1].view(np.uint32)[0]) == b["dbits"], i
+            assert int(s[0, i:i + 1].view(np.uint32)[0]) == b["sbits"], i
 
 
 def test_q8_1_random_both_dtypes():

@@ -6,35 +6,35 @@ import numpy as np
 import oracle
 import workloads
 
-GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-
-
-def _blocks():
-    out, cur = {}, None
-    for line in open(os.path.join(GOLDEN, "q8_1_handmade.txt")):
-        t = line.split("#")[0].split()
-        if not t:
-            continue
-        if t[0] == "block":
-            cur = {"x": np.zeros(32, np.float32), "q": np.zeros(32, np.int64)}
-            out[t[1]] = cur
-        elif t[0] == "end":
-            cur = None
-        elif t[0] in ("d", "s"):
-            cur[t[0]] = float(t[1])
-        else:
-            p = int(t[0])
-            cur["x"][p] = np.float32(float(t[1]))
-            cur["q"][p] = int(t[2])
-    return out
+from tests.golden_files import q8_1_blocks, q8_1_byte_vector
 
 
 def test_handmade_blocks():
-    for name, b in _blocks().items():
+    blocks = q8_1_blocks()
+    assert {"A", "B", "C", "D", "E", "F"} <= set(blocks)
+    for name, b in blocks.items():
         q, d, s = oracle.quantize_q8_1(b["x"][None])
         assert np.array_equal(q[0].astype(np.int64), b["q"]), name
         if "d" in b:
             assert d[0, 0] == np.float32(b["d"]) and s[0, 0] == np.float32(b["s"]), name
+        if "dbits" in b:
+            assert int(d[0, 0:1].view(np.uint32)[0]) == b["dbits"], name
+            assert int(s[0, 0:1].view(np.uint32)[0]) == b["sbits"], name
+
+
+def test_bytes_layout_against_hand_written_vector():
+    """The planar byte layout (quants, then {d, s} per block) against bytes written out by hand."""
+    x, want = q8_1_byte_vector()
+    q, d, s = oracle.quantize_q8_1(x)
+    got = oracle.q8_1_to_bytes(q, d, s)
+    assert got.dtype == np.uint8 and got.size == want.size
+    assert np.array_equal(got, want), f"first mismatch at byte {int(np.argmax(got != want))}"
+    q2, d2, s2 = oracle.q8_1_from_bytes(want, 2, 256)
+    assert q2[0, 0] == 127 and q2[0, 32] == -127 and q2[0, 33] == 2 and q2[1, 40] == -2 and q2[1, 63] == 127
+    assert np.count_nonzero(q2) == 5
+    z = [0.0] * 6
+    assert d2.tolist() == [[1.0, 0.5] + z, [0.0, 2.0] + z]
+    assert s2.tolist() == [[127.0, -62.5] + z, [0.0, 250.0] + z]
 
 
 def test_single_nonzero_block():
