@@ -1,15 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 Q4_K SwiGLU FFN (one JSON line on rank 0).
 
-Workload: the LLaMA-7B-shaped decode FFN (hidden 4096, inter 11008, m = 1,
-seeded Q4_K weights, float32 activations). A step is one full call of the
-feed-forward block (all its kernels). The metric is weight bytes streamed per
-second (GB/s) against the measured HBM copy bandwidth; a secondary object
-reports the 27B-shaped long prefill (hidden 5120, inter 17408, m = 2048) in
-int8-equivalent TOPS against the measured dense fp16/bf16 tensor peak.
+Headline workload: the LLaMA-7B-shaped decode FFN (hidden 4096, inter 11008,
+m = 1, seeded Q4_K weights, float32 activations). A step is one full call of
+the feed-forward block (all its kernels). The metric is weight bytes streamed
+per second (GB/s) against the measured HBM copy bandwidth. Further objects on
+the same line report the other workloads of the method: the tiny decode (256 x
+768), the 13B-shaped batched decode (m = 8, outlier channels), the 8B-shaped
+prefill (m = 512) and the 27B-shaped long prefill (m = 2048), the prefills in
+int8-equivalent TOPS against the measured dense fp16/bf16 tensor peak (burst
+and sustained) and against the int8 mma.sync rate measured in this run; plus
+the Q8_1-activation decode and the Q6_K LM-head GEMV.
 
-Timing: W eager warm-up steps, then K steps replayed from a CUDA graph and
-timed with CUDA events on the capture stream, bracketed by a barrier and a
+Timing: W eager warm-up steps, then exactly K steps replayed from CUDA graphs
+and timed with CUDA events on the capture stream, bracketed by a barrier and a
 device synchronisation on both sides. The weights rotate over enough replicas
 that more than three times the L2 size is touched between two uses of one
 replica, so every step streams its weights from HBM. nvidia-smi samples the
@@ -42,13 +46,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=40000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill-steps", type=int, default=120)
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_1-activation decode leg")
     ap.add_argument("--no-q6k", action="store_true", help="skip the Q6_K LM-head GEMV leg")
+    ap.add_argument("--no-configs", action="store_true", help="skip the tiny, 13B batched and 8B prefill legs")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -137,20 +142,31 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU baseline (oracle)
-def _cpu_decode_worker(budget_s: float, q):
-    import numpy as np
-    import oracle
+def _oracle_call_args(frac_blocks: int | None):
+    """The LLaMA-7B-shaped decode FFN's inputs, or (frac_blocks = b) the same FFN restricted to the
+    first b 256-wide blocks of the intermediate dimension: a sub-problem of the same computation
+    whose cost scales with b (a bounded sample of one call)."""
     import workloads
     cfg = workloads.LLAMA7B_DECODE
     wg, wu, wd = workloads.weights(cfg)
     x, _ = workloads.activations(cfg)
+    if frac_blocks is None:
+        return (x, wg, wu, wd), cfg.weight_bytes()
+    b = frac_blocks
+    wg, wu, wd = wg[:256 * b], wu[:256 * b], wd[:, :b]
+    return (x, wg, wu, wd), (wg.nbytes + wu.nbytes + wd.nbytes)
+
+
+def _cpu_decode_worker(budget_s: float, q):
+    import oracle
+    args, nbytes = _oracle_call_args(None)
     reps, t_total = 0, 0.0
     while t_total < budget_s and reps < 50:
         t = time.perf_counter()
-        oracle.ffn_decode(x, wg, wu, wd)
+        oracle.ffn_decode(*args)
         t_total += time.perf_counter() - t
         reps += 1
-    q.put({"reps": reps, "seconds": t_total, "bytes": cfg.weight_bytes() * reps})
+    q.put({"reps": reps, "seconds": t_total, "bytes": nbytes * reps})
 
 
 def cpu_baseline(budget_s: float):
@@ -168,19 +184,110 @@ def cpu_baseline(budget_s: float):
                       f"single-threaded"}
 
 
+def _reference_worker(steps: int, warmup: int, budget_s: float, q):
+    """`--impl reference`: exactly `warmup` untimed and `steps` timed oracle calls. Each step is one
+    full call when all of them fit in the budget; otherwise each step is the same bounded sample
+    (the FFN restricted to a leading block range of the intermediate dimension)."""
+    import oracle
+    args, nbytes = _oracle_call_args(None)
+    t = time.perf_counter()
+    oracle.ffn_decode(*args)
+    t_call = time.perf_counter() - t
+    blocks = 43                                # 11008 / 256: the whole call
+    if (steps + warmup) * t_call > budget_s:
+        blocks = max(1, int(43 * budget_s / ((steps + warmup) * t_call)))
+        args, nbytes = _oracle_call_args(blocks)
+    for _ in range(max(0, warmup - 1)):
+        oracle.ffn_decode(*args)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.ffn_decode(*args)
+    sec = time.perf_counter() - t0
+    q.put({"steps": steps, "seconds": sec, "bytes": nbytes * steps, "blocks": blocks})
+
+
+def reference_arm(steps: int, warmup: int, budget_s: float = 240.0):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    p = ctx.Process(target=_reference_worker, args=(steps, warmup, budget_s, q))
+    p.start()
+    r = q.get()
+    p.join()
+    return r
+
+
 # --------------------------------------------------------------------------- GPU side
-def gpu_decode(args, rank, world, dist, path="f32"):
-    """Times the decode FFN call: `path` "f32" is ffn_q4k_swiglu (float32 activations),
-    "q8_1" is ffn_q4k_swiglu_q8_1 (activations quantized to Q8_1, integer dot products)."""
-    import numpy as np
+class Steps:
+    """Exactly K calls of `step(i)` (i = 0..K-1, replica i % R) recorded into CUDA graphs: as many
+    replays of a G-step graph as fit, then one graph of the K mod G remaining steps."""
+
+    def __init__(self, step, K: int, R: int, stream):
+        import torch
+        self.K = K
+        self.G = max(1, min(K, R * max(1, 64 // R)))
+        self.full, rem = divmod(K, self.G)
+        self.stream = stream
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    step(i)
+            return g
+        self.g_full = capture(self.G) if self.full else None
+        self.g_rem = capture(rem) if rem else None
+        self.rem = rem
+
+    def replay_all(self, events=None):
+        """Enqueues the K steps; events (full + 2 of them) are recorded before, after each full replay and at the end."""
+        if events:
+            events[0].record(self.stream)
+        for i in range(self.full):
+            self.g_full.replay()
+            if events:
+                events[i + 1].record(self.stream)
+        if self.g_rem is not None:
+            self.g_rem.replay()
+        if events:
+            events[-1].record(self.stream)
+
+
+def _events(n):
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in ev:
+        e.record()  # torch creates the CUDA event on first record
+    return ev
+
+
+def _kernel_ms(q, step, P: int, nk: int):
+    """Mean duration of each of the call's kernels over P calls (events around each kernel;
+    they serialise the kernels, so these are per-kernel, not per-call, figures)."""
+    import torch
+    evs = [_events(2 * nk) for _ in range(P)]
+    torch.cuda.synchronize()
+    for i in range(P):
+        q.q4k_set_profile_events(evs[i])
+        step(i)
+    q.q4k_set_profile_events(None)
+    torch.cuda.synchronize()
+    return [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(nk)]
+
+
+def _gpu_index(dev, world):
+    return os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index if world == 1 else 0].strip()
+
+
+def gpu_decode(cfg, K, warmup, rank, world, dist, path="f32", e2e=False):
+    """Times K decode FFN calls on `cfg`: `path` "f32" is ffn_q4k_swiglu (float32 activations),
+    "q8_1" is ffn_q4k_swiglu_q8_1 (activations quantized to Q8_1)."""
     import torch
     import workloads
     import q4_swiglu_ffn_gb300 as q
 
-    cfg = workloads.LLAMA7B_DECODE
     dev = torch.device("cuda", torch.cuda.current_device())
     wbytes = cfg.weight_bytes()
-    R = max(2, math.ceil(3 * L2_BYTES / wbytes))
+    R = min(64, max(2, math.ceil(3 * L2_BYTES / wbytes)))
     host = [workloads.weights(cfg), workloads.weights(cfg, seed=cfg.seed + 1000)]
     reps = [tuple(torch.from_numpy(a).to(dev) for a in host[r % 2]) for r in range(R)]
     x_np, _ = workloads.activations(cfg)
@@ -201,77 +308,61 @@ def gpu_decode(args, rank, world, dist, path="f32"):
             wg, wu, wd = reps[i % R]
             q.ffn_q4k_swiglu(x, wg, wu, wd, y=y)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(max(3, warmup)):
         step(i)
     torch.cuda.synchronize()
-    G = R * max(1, 64 // R)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            step(i)
-    graph.replay()
+    runs = Steps(step, K, R, stream)
+    runs.replay_all()
     torch.cuda.synchronize()
-    n_rep = max(1, math.ceil(args.steps / G))
-    K = n_rep * G
 
-    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[dev.index if world == 1 else 0]
-    sampler = ClockSampler(gpu_index.strip())
-    time.sleep(0.5)
-    # an event after every replay of G steps: the spread of per-step times
-    evr = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
-    for e in evr:
-        e.record(stream)  # torch creates the CUDA event on first record
+    sampler = ClockSampler(_gpu_index(dev, world))
+    time.sleep(0.3)
+    # a long untimed lead-in keeps the clocks at their loaded value into the timed region
+    lead = Steps(step, max(K, 2000), R, stream) if K < 2000 else runs
+    ev = _events(runs.full + 2)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    evr[0].record(stream)
-    for i in range(n_rep):
-        graph.replay()
-        evr[i + 1].record(stream)
+    lead.replay_all()
+    runs.replay_all(ev)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist:
         dist.barrier()
+    ms = ev[0].elapsed_time(ev[-1])
+    per_step = sorted(ev[i].elapsed_time(ev[i + 1]) / runs.G for i in range(runs.full)) or [ms / K]
+    n = len(per_step)
+    pct = {p: per_step[min(n - 1, int(p / 100 * n))] for p in (10, 50, 90)}
+    # a longer timed run beside the K steps: many steps, so the spread and clocks mean something
+    long_ms, long_K = None, 0
+    if K < 2000:
+        ev2 = _events(lead.full + 2)
+        lead.replay_all(ev2)
+        torch.cuda.synchronize()
+        long_ms, long_K = ev2[0].elapsed_time(ev2[-1]), lead.K
+    t2 = time.time()
     sampler.stop()
-    ms = evr[0].elapsed_time(evr[-1])
-    per_step = sorted(evr[i].elapsed_time(evr[i + 1]) / G for i in range(n_rep))
-    pct = {q: per_step[min(n_rep - 1, int(q / 100 * n_rep))] for q in (10, 50, 90)}
-    clocks = sampler.summary(t0, t1)
-
-    # per-kernel durations (events around each kernel of the call; serialises them)
-    nk = 5
-    P = 300
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
-    for ev in evs:
-        for e in ev:
-            e.record(stream)  # torch creates the CUDA event on first record
-    torch.cuda.synchronize()
-    for i in range(P):
-        q.q4k_set_profile_events(evs[i])
-        step(i)
-    q.q4k_set_profile_events(None)
-    torch.cuda.synchronize()
-    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(nk)]
-
-    # end to end, every step through the C ABI with host buffers and a stream sync:
-    # (a) x and y in page-locked host memory, read and written by the kernels across
-    #     the host link (no separate copies); (b) explicit copies: pinned x -> device,
-    #     the call, device y -> pinned host.
-    xh = torch.from_numpy(x_np).pin_memory()
-    yh = torch.empty(x_np.shape, dtype=torch.float32).pin_memory()
-    E = min(K, 2000) if path == "f32" else 0
-
-    def host_step(i):
-        wg, wu, wd = reps[i % R]
-        q.ffn_q4k_swiglu(xh, wg, wu, wd, y=yh)
+    clocks = sampler.summary(t0, t2)
+    kern_ms = _kernel_ms(q, step, 300, 5)
 
     e2e_ms = e2e_copy_ms = 0.0
+    E = min(max(K, 200), 2000) if e2e else 0
+    xh = torch.from_numpy(x_np).pin_memory()
+    yh = torch.empty(x_np.shape, dtype=torch.float32).pin_memory()
     if E:
+        # end to end, every step through the C ABI with host buffers and a stream sync:
+        # (a) x and y in page-locked host memory, read and written by the kernels across
+        #     the host link (no separate copies); (b) explicit copies: pinned x -> device,
+        #     the call, device y -> pinned host.
+        def host_step(i):
+            wg, wu, wd = reps[i % R]
+            q.ffn_q4k_swiglu(xh, wg, wu, wd, y=yh)
+
         for i in range(3):
             host_step(i)
         torch.cuda.synchronize()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0, f1 = _events(2)
         f0.record(stream)
         for i in range(E):
             host_step(i)
@@ -291,12 +382,14 @@ def gpu_decode(args, rank, world, dist, path="f32"):
     assert q.q4k_check_device_error() == 0
     step(0)
     launches = q.q4k_last_call_kernels()
-    return {"ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms, "e2e_copy_ms": e2e_copy_ms,
-            "E": E, "R": R,
-            "wbytes": wbytes, "xbytes": x_np.nbytes, "launches_per_step": launches, "pct": pct, "G": G}
+    torch.cuda.synchronize()
+    torch.cuda.set_stream(torch.cuda.default_stream())
+    return {"cfg": cfg, "ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms,
+            "e2e_copy_ms": e2e_copy_ms, "E": E, "R": R, "wbytes": wbytes, "xbytes": x_np.nbytes,
+            "launches_per_step": launches, "pct": pct, "G": runs.G, "long_ms": long_ms, "long_K": long_K}
 
 
-def gpu_q6k(args):
+def gpu_q6k(K):
     """The Q6_K LM-head GEMV (LLaMA-7B output projection, m = 1), graph-replayed like the decode."""
     import torch
     import workloads
@@ -317,91 +410,90 @@ def gpu_q6k(args):
     def step(i):
         q.q6k_gemv(x, reps[i % R], ws, y=y)
 
-    for i in range(max(3, args.warmup)):
+    for i in range(3):
         step(i)
     torch.cuda.synchronize()
-    G = R * max(1, 64 // R)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            step(i)
-    graph.replay()
+    runs = Steps(step, K, R, stream)
+    runs.replay_all()
+    ev = _events(runs.full + 2)
+    runs.replay_all(ev)
     torch.cuda.synchronize()
-    n_rep = max(3, math.ceil(args.steps / 4 / G))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n_rep):
-        graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / (n_rep * G)
-    P = 200
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(P)]
-    for ev in evs:
-        for e in ev:
-            e.record(stream)
-    torch.cuda.synchronize()
-    for i in range(P):
-        q.q4k_set_profile_events(evs[i])
-        step(i)
-    q.q4k_set_profile_events(None)
-    torch.cuda.synchronize()
-    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(2)]
+    ms = ev[0].elapsed_time(ev[-1]) / K
+    kern_ms = _kernel_ms(q, step, 200, 2)
     assert q.q4k_check_device_error() == 0
-    return {"cfg": c, "ms": ms, "K": n_rep * G, "kern_ms": kern_ms, "wbytes": wbytes, "R": R}
+    torch.cuda.set_stream(torch.cuda.default_stream())
+    return {"cfg": c, "ms": ms, "K": K, "kern_ms": kern_ms, "wbytes": wbytes, "R": R}
 
 
-def gpu_prefill(args):
+def gpu_prefill(cfg, steps, world):
+    import numpy as np
     import torch
     import workloads
     import q4_swiglu_ffn_gb300 as q
 
-    cfg = workloads.LONG_PREFILL_27B
     dev = torch.device("cuda", torch.cuda.current_device())
     wg, wu, wd = (torch.from_numpy(a).to(dev) for a in workloads.weights(cfg))
     _, xb = workloads.activations(cfg)
-    import numpy as np
     x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
     m, H, I = cfg.m, cfg.hidden, cfg.inter
     ws = torch.zeros(q.ffn_q4k_workspace_bytes(m, H, I), dtype=torch.uint8, device=dev)
     y = torch.empty((m, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(i=0):
         q.ffn_q4k_swiglu_ex(x, wg, wu, wd, ws, y=y)
 
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    gpu_index = os.environ.get("CUDA_VISIBLE_DEVICES", str(dev.index)).split(",")[0]
-    sampler = ClockSampler(gpu_index.strip())
+    sampler = ClockSampler(_gpu_index(dev, world))
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = _events(2)
     t0 = time.time()
     e0.record(stream)
-    for _ in range(args.prefill_steps):
+    for _ in range(steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    ms = e0.elapsed_time(e1) / args.prefill_steps
-    nk = 5
-    P = 10
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * nk)] for _ in range(P)]
-    for ev in evs:
-        for e in ev:
-            e.record(stream)  # torch creates the CUDA event on first record
-    torch.cuda.synchronize()
-    for i in range(P):
-        q.q4k_set_profile_events(evs[i])
-        step()
-    q.q4k_set_profile_events(None)
-    torch.cuda.synchronize()
-    kern_ms = [sum(evs[i][2 * k].elapsed_time(evs[i][2 * k + 1]) for i in range(P)) / P for k in range(nk)]
+    ms = e0.elapsed_time(e1) / steps
+    kern_ms = _kernel_ms(q, step, 30, 5)
+    step()
+    launches = q.q4k_last_call_kernels()
     assert q.q4k_check_device_error() == 0
-    return {"ms": ms, "kern_ms": kern_ms, "ops": cfg.int8_ops(), "cfg": cfg, "clocks": clocks}
+    return {"ms": ms, "kern_ms": kern_ms, "ops": cfg.int8_ops(), "cfg": cfg, "clocks": clocks, "steps": steps,
+            "launches_per_step": launches, "timed_s": t1 - t0}
+
+
+def gpu_int8_peak(world):
+    """The int8 tensor rate of this part (mma.sync m16n8k32 s8), measured now: best of 5 launches."""
+    import torch
+    import q4_swiglu_ffn_gb300 as q
+    dev = torch.device("cuda", torch.cuda.current_device())
+    iters = 8192
+    for _ in range(2):
+        q.q4k_bench_int8_mma(iters)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(_gpu_index(dev, world))
+    time.sleep(0.3)
+    best = None
+    t0 = time.time()
+    for _ in range(5):
+        e0, e1 = _events(2)
+        e0.record()
+        ops = q.q4k_bench_int8_mma(iters)
+        e1.record()
+        torch.cuda.synchronize()
+        tops = ops / (e0.elapsed_time(e1) * 1e-3) / 1e12
+        best = tops if best is None else max(best, tops)
+    t1 = time.time()
+    sampler.stop()
+    assert q.q4k_check_device_error() == 0
+    return {"tops": best, "instruction": "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32",
+            "how": "best of 5 launches, 4 CTAs x 8 warps per SM, 8 independent MMA chains per warp, CUDA events",
+            "clocks": sampler.summary(t0, t1)}
 
 
 def whole_job(ms_local: float, units_local: float, dist=None):
@@ -416,6 +508,61 @@ def whole_job(ms_local: float, units_local: float, dist=None):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return ms, units_local * world / (ms * 1e-3)
+
+
+DECODE_KERNELS = ["prep_x", "gate_up", "swiglu_frag_h", "down", "down_chunk_sum"]
+Q8_KERNELS = ["q8_1_x", "gate_up", "swiglu_q8_1_h", "down", "down_chunk_sum"]
+PREFILL_KERNELS = ["q8_1_x", "expand_x", "gate_up_mmq", "expand_h", "down_mmq_and_sums"]
+DECODE_DTYPE = "f16 hi+lo x (~22-bit), exact f16 q*scale weights, f32 accumulate"
+
+
+def decode_object(r, pk, pk_kind, names, dtype, kernel_label):
+    """The JSON object of one decode leg: rate, per-kernel times and the roofline of the gate/up GEMV."""
+    c = r["cfg"]
+    k1_bytes = 2 * c.inter * (c.hidden // 256) * 144
+    k1_ms = r["kern_ms"][1]
+    ach = k1_bytes / (k1_ms * 1e-3) / 1e9
+    step_ms = r["ms"] / r["K"]
+    o = {"workload": c.name, "hidden": c.hidden, "inter": c.inter, "m": c.m,
+         "value": r["wbytes"] / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "steps": r["K"], "ms_per_step": step_ms,
+         "step_frac": (r["wbytes"] / (step_ms * 1e-3) / 1e9) / pk["hbm_gbs"], "dtype": dtype,
+         "kernels_ms": dict(zip(names, r["kern_ms"][:r["launches_per_step"]])),
+         "roofline": {"kernel": kernel_label, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
+                      "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth",
+                      "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_ms": k1_ms},
+         "l2": f"rotating {r['R']} weight replicas ({r['R'] * r['wbytes'] / 1e6:.1f} MB)"
+               + (" > 3x the L2" if r["R"] * r["wbytes"] > 3 * L2_BYTES else ", L2-resident: launch-bound size"),
+         "gpu_launches": r["launches_per_step"] * r["K"], "clocks": r["clocks"]}
+    if r["long_ms"]:
+        o["long_run"] = {"steps": r["long_K"], "ms_per_step": r["long_ms"] / r["long_K"],
+                         "value": r["wbytes"] * r["long_K"] / (r["long_ms"] * 1e-3) / 1e9}
+    return o
+
+
+def prefill_object(pre, pk, pk_kind, int8):
+    c = pre["cfg"]
+    gu_ops = 2 * c.m * c.hidden * c.inter * 2
+    gu_ms = pre["kern_ms"][2]
+    ach = gu_ops / (gu_ms * 1e-3) / 1e12
+    burst, sus = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
+    o = {"workload": c.name, "hidden": c.hidden, "inter": c.inter, "m": c.m,
+         "value": pre["ops"] / (pre["ms"] * 1e-3) / 1e12, "unit": "TOPS (int8-equivalent)",
+         "ms_per_step": pre["ms"], "steps": pre["steps"], "timed_s": pre["timed_s"],
+         "dtype": "f16 tcgen05 (exact f16 q*scale weights, Q8_1 activations as f16 hi+lo), f32 accumulate",
+         "kernels_ms": dict(zip(PREFILL_KERNELS, pre["kern_ms"])),
+         "roofline": {"kernel": "mmq_kernel<gate+up> (tcgen05 kind::f16)", "bound": "tensor",
+                      "achieved": ach, "peak": burst, "unit": "TFLOP/s", "frac": ach / burst,
+                      "peak_kind": f"{pk_kind} burst dense bf16 (the fp16 tensor rate is the same)",
+                      "frac_sustained": ach / sus, "peak_sustained": sus,
+                      "executed_fp16_frac": 2 * ach / burst, "avg_launch_ms": gu_ms,
+                      "algorithmic_ops_per_launch": gu_ops,
+                      "note": "achieved counts the algorithmic int8-equivalent ops; the kernel executes 2x "
+                              "that in fp16 (activations split into hi+lo)"},
+         "gpu_launches": pre["launches_per_step"] * pre["steps"], "clocks": pre["clocks"]}
+    if int8 is not None:
+        o["vs_int8_mma_sync"] = {"int8_peak_tops": int8["tops"], "call_frac": o["value"] / int8["tops"],
+                                 "gate_up_frac": ach / int8["tops"]}
+    return o
 
 
 def main():
@@ -433,12 +580,19 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        cb = cpu_baseline(args.cpu_budget_s)
-        v = cb["value"]
+        r = reference_arm(args.steps, args.warmup)
+        v = r["bytes"] / r["seconds"] / 1e9
+        whole = r["blocks"] == 43
+        sample = (f"{r['steps']} timed calls of the numpy float64 oracle on the whole LLaMA-7B-shaped decode FFN "
+                  f"(m=1), {args.warmup} untimed" if whole else
+                  f"{r['steps']} timed calls of the numpy float64 oracle, each on the same bounded sample of the "
+                  f"LLaMA-7B-shaped decode FFN: intermediate rows 0..{256 * r['blocks'] - 1} of 11008")
         line = {"impl": "reference", "metric": metric, "value": v, "unit": "GB/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cfg.weight_bytes() / (v * 1e9) * 1e3,
+                "steps": r["steps"], "warmup": args.warmup, "ms_per_step": r["seconds"] / r["steps"] * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": workload, "cpu_baseline": cb,
+                "data": "synthetic", "config": workload,
+                "cpu_baseline": {"value": v, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                                 "sample": sample},
                 "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -456,51 +610,45 @@ def main():
         import __graft_entry__
         __graft_entry__.build()
 
-    r = gpu_decode(args, rank, world, dist)
+    K = max(1, args.steps)
+    r = gpu_decode(cfg, K, args.warmup, rank, world, dist, e2e=True)
     ms, rate = whole_job(r["ms"], r["wbytes"] * r["K"], dist)
     value = rate / 1e9
     pk, pk_kind = peaks()
+    lead = rank == 0
 
-    r8 = None
-    if not args.no_q8 and rank == 0:
-        r8 = gpu_decode(args, rank, 1, None, path="q8_1")
+    r8 = gpu_decode(cfg, 2000, 3, rank, 1, None, path="q8_1") if (lead and not args.no_q8) else None
+    r6 = gpu_q6k(1000) if (lead and not args.no_q6k) else None
+    others = {}
+    if lead and not args.no_configs:
+        others["decode_tiny_h256_i768_m1"] = gpu_decode(workloads.TINY_DECODE, 2000, 3, rank, 1, None)
+        others["decode_13b_h5120_i13824_m8"] = gpu_decode(workloads.BATCHED_13B_DECODE, 2000, 3, rank, 1, None)
+    int8 = gpu_int8_peak(1) if (lead and not args.no_prefill) else None
+    pre = {}
+    if lead and not args.no_prefill:
+        if not args.no_configs:
+            pre["prefill_8b_h4096_i14336_m512"] = gpu_prefill(workloads.PREFILL_8B, 4 * args.prefill_steps, 1)
+        pre["prefill_27b_h5120_i17408_m2048"] = gpu_prefill(workloads.LONG_PREFILL_27B, args.prefill_steps, 1)
+    cb = cpu_baseline(args.cpu_budget_s) if (lead and world == 1) else None
 
-    r6 = None
-    if not args.no_q6k and rank == 0:
-        r6 = gpu_q6k(args)
-
-    pre = None
-    if not args.no_prefill and rank == 0:
-        pre = gpu_prefill(args)
-    cb = cpu_baseline(args.cpu_budget_s) if (rank == 0 and world == 1) else None
-
-    if rank != 0:
+    if not lead:
         if dist:
             dist.destroy_process_group()
         return
-    # dominant kernel: gate+up GEMV (2/3 of the weight bytes)
-    k1_bytes = 2 * cfg.inter * (cfg.hidden // 256) * 144
-    k1_ms = r["kern_ms"][1]
-    ach = k1_bytes / (k1_ms * 1e-3) / 1e9
-    sha = src_hash("decode.cu", "common.cuh")
-    roof = {"kernel": "gemv_kernel<gate/up> (K1)", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth",
-            "traffic": profiled_traffic("decode_gateup_llama7b_m1.txt", sha),
-            "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_ms": k1_ms,
-            "step_frac": (r["wbytes"] / (ms / r["K"] * 1e-3) / 1e9) / pk["hbm_gbs"]}
+    head = decode_object(r, pk, pk_kind, DECODE_KERNELS, DECODE_DTYPE, "gemv_kernel<gate/up> (K1)")
+    roof = dict(head["roofline"])
+    roof["traffic"] = profiled_traffic("decode_gateup_llama7b_m1.txt", src_hash("decode.cu", "common.cuh"))
+    roof["step_frac"] = head["step_frac"]
     e2e_val = r["wbytes"] * r["E"] / (r["e2e_ms"] * 1e-3) / 1e9
     line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": r["K"],
             "warmup": args.warmup, "ms_per_step": ms / r["K"],
             "ms_per_step_p10_p50_p90": [r["pct"][10], r["pct"][50], r["pct"][90]],
             "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f16",
+            "vs_baseline": None, "dtype": DECODE_DTYPE,
             "data": "synthetic",
-            "config": dict(workload, l2=f"rotating {r['R']} weight replicas ({r['R'] * r['wbytes'] / 1e6:.0f} MB "
-                                        f"> 3x the {L2_BYTES / 1e6:.0f} MB L2)", graph="CUDA graph replay",
-                           parallelism=f"replicas x{world}"),
+            "config": dict(workload, l2=head["l2"], graph="CUDA graph replay", parallelism=f"replicas x{world}"),
             "roofline": roof,
-            "kernels_ms": dict(zip(["prep_x", "gate_up", "swiglu_frag_h", "down", "down_chunk_sum"],
-                                   r["kern_ms"][:r["launches_per_step"]])),
+            "kernels_ms": head["kernels_ms"],
             "cpu_baseline": cb,
             "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": r["xbytes"],
                     "d2h_bytes_per_step": r["xbytes"], "steps": r["E"],
@@ -511,25 +659,16 @@ def main():
                                             "stream sync, every step"}},
             "gpu_launches": r["launches_per_step"] * r["K"] * world,
             "clocks": r["clocks"]}
+    if r["long_ms"]:
+        line["long_run"] = head["long_run"]
+    for key, ro in others.items():
+        line[key] = decode_object(ro, pk, pk_kind, DECODE_KERNELS, DECODE_DTYPE, "gemv_kernel<gate/up> (K1)")
     if r8 is not None:
-        k1q_ms = r8["kern_ms"][1]
-        ach8 = k1_bytes / (k1q_ms * 1e-3) / 1e9
-        line["decode_q8_1"] = {
-            "workload": cfg.name, "value": r8["wbytes"] * r8["K"] / (r8["ms"] * 1e-3) / 1e9, "unit": "GB/s",
-            "ms_per_step": r8["ms"] / r8["K"],
-            "ms_per_step_p10_p50_p90": [r8["pct"][10], r8["pct"][50], r8["pct"][90]],
-            "step_frac": (r8["wbytes"] / (r8["ms"] / r8["K"] * 1e-3) / 1e9) / pk["hbm_gbs"],
-            "dtype": "int8 x u4 (dp4a), f32 scales",
-            "numerics": "activations quantized to Q8_1 (x once for gate and up, h before down): "
-                        "not the float32-activation contract of the headline value",
-            "kernels_ms": dict(zip(["q8_1_x", "gate_up", "swiglu_q8_1_h", "down", "down_chunk_sum"],
-                                   r8["kern_ms"][:r8["launches_per_step"]])),
-            "roofline": {"kernel": "gemv_q8_kernel<gate/up> (K1)", "bound": "hbm", "achieved": ach8,
-                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach8 / pk["hbm_gbs"],
-                         "peak_kind": f"{pk_kind} copy bandwidth", "algorithmic_bytes_per_launch": k1_bytes,
-                         "avg_launch_ms": k1q_ms},
-            "gpu_launches": r8["launches_per_step"] * r8["K"],
-            "clocks": r8["clocks"]}
+        o = decode_object(r8, pk, pk_kind, Q8_KERNELS, "Q8_1 activations: int8 x u4 dp4a (m <= 2), f32 scales",
+                          "gemv_q8_kernel<gate/up> (K1)")
+        o["numerics"] = ("activations quantized to Q8_1 (x once for gate and up, h before down): "
+                         "not the float32-activation contract of the headline value")
+        line["decode_q8_1"] = o
     if r6 is not None:
         c6 = r6["cfg"]
         ach6 = r6["wbytes"] / (r6["kern_ms"][1] * 1e-3) / 1e9
@@ -542,24 +681,10 @@ def main():
                          "algorithmic_bytes_per_launch": r6["wbytes"], "avg_launch_ms": r6["kern_ms"][1]},
             "step_frac": (r6["wbytes"] / (r6["ms"] * 1e-3) / 1e9) / pk["hbm_gbs"],
             "l2": f"rotating {r6['R']} weight replicas"}
-    if pre is not None:
-        c = pre["cfg"]
-        gu_ops = 2 * c.m * c.hidden * c.inter * 2
-        gu_ms = pre["kern_ms"][2]
-        peak_t = pk["bf16_tflops_sustained"]  # a long run of back-to-back calls, as the sustained GEMM
-        line["prefill"] = {
-            "workload": c.name, "value": pre["ops"] / (pre["ms"] * 1e-3) / 1e12, "unit": "TOPS (int8-equivalent)",
-            "ms_per_step": pre["ms"],
-            "kernels_ms": dict(zip(["q8_1_x", "expand_x", "gate_up_mmq", "expand_h", "down_mmq"], pre["kern_ms"])),
-            "roofline": {"kernel": "mmq_kernel<gate+up> (tcgen05 kind::f16)", "bound": "tensor",
-                         "achieved": gu_ops / (gu_ms * 1e-3) / 1e12, "peak": peak_t, "unit": "TFLOP/s",
-                         "frac": gu_ops / (gu_ms * 1e-3) / 1e12 / peak_t,
-                         "peak_kind": f"{pk_kind} sustained dense bf16 (same tensor rate as fp16)",
-                         "executed_fp16_frac": 2 * gu_ops / (gu_ms * 1e-3) / 1e12 / peak_t,
-                         "note": "achieved counts the algorithmic int8-equivalent ops; the kernel executes 2x "
-                                 "that in fp16 (activations split into hi+lo)"},
-            "clocks": pre["clocks"],
-            "int8_mma_sync_peak_tops": 151.7}
+    if int8 is not None:
+        line["int8_tensor_peak"] = int8
+    for key, p in pre.items():
+        line[key] = prefill_object(p, pk, pk_kind, int8)
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

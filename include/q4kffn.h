@@ -260,6 +260,17 @@ q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream);
  * whole call leave the hook off. */
 q4k_status q4k_set_profile_events(void* const* events, int n);
 
+/* Benchmark hook (no counterpart on the source pages): the int8 tensor-core
+ * rate. Enqueues on `stream` one kernel in which every warp issues `iters`
+ * rounds of 8 independent mma.sync.m16n8k32 s8 x s8 -> s32 operations (the
+ * int8 tensor instruction of sm_103a; tcgen05.mma has no integer kind here) and
+ * nothing else, 4 CTAs of 8 warps per SM. *ops_per_launch receives the integer
+ * operations the launch performs (2*16*8*32 per MMA); the caller times the
+ * launch (CUDA events on `stream`) and divides. iters in 1..2^24, else
+ * Q4K_ERR_SHAPE; ops_per_launch NULL gives Q4K_ERR_NULL. Touches no memory of
+ * the caller. */
+q4k_status q4k_bench_int8_mma(int64_t iters, double* ops_per_launch, q4k_stream_t stream);
+
 /* Benchmark hook: how many kernels the most recent FFN or Q6_K GEMV call on
  * this thread launched (directly, or as nodes of the replayed graph). */
 int q4k_last_call_kernels(void);

@@ -50,6 +50,7 @@ _SIGS = {
     "q4k_get_last_error": (_int, []),
     "q4k_last_call_kernels": (_int, []),
     "q4k_status_string": (ctypes.c_char_p, [_int]),
+    "q4k_bench_int8_mma": (_int, [_i64, ctypes.POINTER(ctypes.c_double), _p]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -247,6 +248,13 @@ _prof_keep = None
 def q4k_last_call_kernels() -> int:
     """Kernels the last FFN or Q6_K GEMV call on this thread launched (benchmark hook)."""
     return lib.q4k_last_call_kernels()
+
+
+def q4k_bench_int8_mma(iters: int, stream=None) -> float:
+    """Enqueues the int8 tensor-rate kernel; returns the integer operations of the launch (benchmark hook)."""
+    ops = ctypes.c_double(0.0)
+    _check(lib.q4k_bench_int8_mma(iters, ctypes.byref(ops), _stream(stream)), "q4k_bench_int8_mma")
+    return ops.value
 
 
 def q4k_get_last_error() -> int:
