@@ -76,9 +76,10 @@ def src_hash(*files) -> str:
     for f in files:
         text = open(os.path.join(ROOT, "q4_swiglu_ffn_gb300", "csrc", f)).read()
         if f == "decode.cu":
-            a = text.index("template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>")
-            b = text.index("constexpr size_t gemv_smem()")
-            text = text[a:b]
+            a = text.find("template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS")
+            b = text.find("constexpr size_t gemv_smem()")
+            if 0 <= a < b:
+                text = text[a:b]
         text = re.sub(r"//[^\n]*", "", text)
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         h.update(re.sub(r"\s+", "", text).encode())

@@ -123,6 +123,59 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
   if (lane == 0) f.sc[(int64_t)sb * sc_stride(nt) + t] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
+// One token (m = 1): block-diagonal B. Quad thread tig of an MMA owns quant
+// group tig of every row (sub-blocks 2tig and 2tig+1) and supplies 4 of its
+// weights per row and MMA as fp16 subnormals q * 2^-24 (low nibbles) or
+// 16q * 2^-24 (high nibbles), straight from the quant word with one AND. The
+// B column pair (2tig, 2tig+1) holds the hi and lo parts of x at exactly those
+// k rows and is zero elsewhere, so C column pair tig collects sub-block
+// 2tig's (or 2tig+1's) partial dot product alone and the 6-bit scale is
+// applied once per superblock in float32. MMA index k: 0..7 = low nibbles of
+// quant bytes 4k..4k+3 of the group, 8..15 = their high nibbles. Layout per
+// superblock: fx [16 MMAs][8 lanes with data: lane 4g + (g >> 1)] uint2 (b0 = x
+// at bytes 0 and 2 of the word, b1 = x at bytes 1 and 3; g = 2tig + part), fm as
+// float [8] sub-block sums of x * 2^-e, sc [1] 2^e. Lane L holds x[8L .. 8L+7]
+// of the superblock: quant group L >> 3, nibble half (L >> 2) & 1, MMAs
+// 2(L & 3) and 2(L & 3) + 1.
+__device__ __forceinline__ void frag_token_diag(const float v_in[8], int sb, FragPtrs f) {
+  const int lane = threadIdx.x & 31;
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v_in[i]));
+  amax = warp_max(amax);
+  int e = 0;
+  if (amax > 0.f) e = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100);
+  const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  __half hi[8], lo[8];
+  float xsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = v_in[i] * s;
+    hi[i] = __float2half_rn(y);
+    lo[i] = __float2half_rn(y - __half2float(hi[i]));
+    xsum += y;
+  }
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);  // lanes 4j .. 4j+3 hold sub-block j
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+  float* X = reinterpret_cast<float*>(f.fm) + (int64_t)sb * 8;
+  if ((lane & 3) == 0) X[lane >> 2] = xsum;
+  const int tig = lane >> 3, half = (lane >> 2) & 1, s0 = 2 * (lane & 3);
+  uint2* fx = f.fx + (int64_t)sb * 16 * 8;
+#pragma unroll
+  for (int ss = 0; ss < 2; ++ss) {
+    const int k = half * 8 + s0 + ss;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const __half* h8 = part ? lo : hi;
+      uint2 fr;
+      fr.x = h2_as_u32(__halves2half2(h8[4 * ss + 0], h8[4 * ss + 2]));
+      fr.y = h2_as_u32(__halves2half2(h8[4 * ss + 1], h8[4 * ss + 3]));
+      fx[k * 8 + 2 * tig + part] = fr;
+    }
+  }
+  if (lane == 0) f.sc[sb] = __uint_as_float((uint32_t)(127 + e) << 23);
+}
+
 // Loads the 8 inputs of this lane (float32 or bf16, widened exactly).
 __device__ __forceinline__ void load8(const float* p, float v[8]) {
   const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
@@ -147,8 +200,9 @@ __device__ __forceinline__ void round_q8_1(float v[8], int8_t q[8], float& d, fl
   for (int i = 0; i < 8; ++i) v[i] = (float)q[i] * d;
 }
 
-// K0: one CTA per superblock of x, one warp per token slot.
-template <typename T, bool Q8>
+// K0: one CTA per superblock of x, one warp per token slot (DIAG: one token,
+// block-diagonal fragments).
+template <typename T, bool Q8, bool DIAG = false>
 __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f) {
   pdl_launch_dependents();
   const int t = threadIdx.x >> 5, sb = blockIdx.x, lane = threadIdx.x & 31;
@@ -161,7 +215,10 @@ __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt
       round_q8_1(v, q, d, s);
     }
   }
-  frag_token(v, t >= m, t, nt, sb, f);
+  if constexpr (DIAG)
+    frag_token_diag(v, sb, f);
+  else
+    frag_token(v, t >= m, t, nt, sb, f);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
@@ -169,7 +226,7 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 // K1b: one CTA per 256-row block of h, one warp per token slot. Sums the
 // gate/up chunks in order, applies SwiGLU and writes the fragments of h (Q8: of
 // Q8_1(h), whose quants and (d, s) also go to hq [m][inter] and hds [m][inter/32]).
-template <bool Q8>
+template <bool Q8, bool DIAG = false>
 __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, int m, int inter, int nt, FragPtrs f,
                                      uint8_t* __restrict__ hq, float2* __restrict__ hds) {
   pdl_launch_dependents();
@@ -204,7 +261,10 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
       if ((lane & 3) == 0) hds[((int64_t)t * inter + i0) / Q8B] = make_float2(d, s);
     }
   }
-  frag_token(v, t >= m, t, nt, sb, f);
+  if constexpr (DIAG)
+    frag_token_diag(v, sb, f);
+  else
+    frag_token(v, t >= m, t, nt, sb, f);
 }
 
 struct GemvParams {
@@ -216,6 +276,7 @@ struct GemvParams {
   FragPtrs in;        // B fragments of the input
   float* out;         // chunk sums: [nks][2][m][rows] (gate/up) or [nks][m][rows] (down)
   uint32_t* err;
+  int diag;           // one token with block-diagonal B fragments (frag_token_diag)
 };
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -230,10 +291,11 @@ __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, u
 // COMBOS 16-row tiles per superblock and step (gate and up of the same rows, or
 // COMBOS consecutive tiles of W_down); each warp takes TPW of them (sharing the
 // B operand) at one of the SLICES superblocks.
-template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS>
+template <bool GATEUP, int NT, int COMBOS, int TPW, int SLICES, int STAGES, int CPS, bool DIAG>
 __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     gemv_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
                 const GemvParams P) {
+  static_assert(!DIAG || NT == 1, "the block-diagonal operand carries one token");
   constexpr int TG = COMBOS / TPW;  // tile groups
   constexpr int WARPS = TG * SLICES;
   static_assert(COMBOS % TPW == 0, "tiles split evenly over warps");
@@ -352,6 +414,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   uint2 bc[CACHEB ? 16 : 1][NT];
   uint32_t bmc[NT];
   float xsc[NT];
+  float xlo = 0.f, xhi = 0.f;  // DIAG: sums of x * 2^-e over sub-blocks 2tig and 2tig+1
   int csb = -1;
 
   // A warp whose wait timed out raises the CTA's abort flag and stops waiting,
@@ -377,7 +440,64 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     }
     const int sb = cw.g * SLICES + slice;
     const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
-    if (!failed && sb < chunk_end) {
+    if (DIAG && !failed && sb < chunk_end) {
+      // ------------------------------------------ TPW 16-row tiles of one superblock, one token
+      if (sb != csb) {
+        const uint2* fxd = P.in.fx + (int64_t)sb * 16 * 8;
+        const bool act = (g >> 1) == tig;  // this lane's B column pair belongs to its own quant group
+#pragma unroll
+        for (int k = 0; k < 16; ++k) bc[k][0] = act ? fxd[k * 8 + g] : make_uint2(0u, 0u);
+        const float* X = reinterpret_cast<const float*>(P.in.fm) + (int64_t)sb * 8;
+        xlo = X[2 * tig];
+        xhi = X[2 * tig + 1];
+        xsc[0] = P.in.sc[sb] * 1048576.f;  // 2^e * 2^20
+        csb = sb;
+      }
+#pragma unroll
+      for (int t = 0; t < TPW; ++t) {
+        const int cb = tgrp * TPW + t;
+        const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
+                                                                 : (slice * RU + cb * ROWS) * BLK);
+        uint4 hd[2], q0[2], q1[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const uint8_t* rb = base + (g + 8 * r) * BLK;
+          hd[r] = *reinterpret_cast<const uint4*>(rb);
+          q0[r] = *reinterpret_cast<const uint4*>(rb + 16 + 32 * tig);
+          q1[r] = *reinterpret_cast<const uint4*>(rb + 32 + 32 * tig);
+        }
+        // clo: sub-block 2tig (low nibbles, q * 2^-24); chi: sub-block 2tig+1 (high nibbles, q * 2^-20).
+        // Columns 2tig and 2tig+1 hold the hi and lo parts of x.
+        float clo[4] = {0.f, 0.f, 0.f, 0.f}, chi[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+          const uint4& qa = (w < 4) ? q0[0] : q1[0];
+          const uint4& qb = (w < 4) ? q0[1] : q1[1];
+          const uint32_t w0 = (w & 3) == 0 ? qa.x : (w & 3) == 1 ? qa.y : (w & 3) == 2 ? qa.z : qa.w;
+          const uint32_t w1 = (w & 3) == 0 ? qb.x : (w & 3) == 1 ? qb.y : (w & 3) == 2 ? qb.z : qb.w;
+          const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
+          mma16816(clo, w0 & 0x000F000Fu, w1 & 0x000F000Fu, t0 & 0x000F000Fu, t1 & 0x000F000Fu, bc[w][0].x,
+                   bc[w][0].y);
+          mma16816(chi, w0 & 0x00F000F0u, w1 & 0x00F000F0u, t0 & 0x00F000F0u, t1 & 0x00F000F0u, bc[8 + w][0].x,
+                   bc[8 + w][0].y);
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          // (scale, scale) and (min, min) of sub-blocks 2tig and 2tig+1 as fp16 1024 + value
+          const uint32_t ps = prmt(hd[r].y, hd[r].w, selM), pm = prmt(hd[r].z, hd[r].w, selM);
+          const uint32_t scb = lop3_and_or(ps, mL, lop3_and_or(ps >> 10, mH, 0x64006400u));
+          const uint32_t mnb = lop3_and_or(pm >> sM, mL, lop3_and_or(pm >> 10, mH, 0x64006400u));
+          // (16 * scale_2tig, scale_2tig+1) and (min_2tig, min_2tig+1), exact
+          const float2 sf = __half22float2(__hfma2(u32_as_h2(scb), u32_as_h2(0x3C004C00u), u32_as_h2(0xE400F400u)));
+          const float2 mf = __half22float2(__hsub2(u32_as_h2(mnb), u32_as_h2(0x64006400u)));
+          const float2 dd = __half22float2(u32_as_h2(hd[r].x));
+          const float tq = fmaf(sf.y, chi[2 * r] + chi[2 * r + 1], sf.x * (clo[2 * r] + clo[2 * r + 1]));
+          const float tm = fmaf(mf.y, xhi, mf.x * xlo);
+          const float S = fmaf(dd.x, tq, -(dd.y * 9.5367431640625e-07f) * tm);  // dmin * 2^-20
+          acc[t][0][r] = fmaf(S, xsc[0], acc[t][0][r]);
+        }
+      }
+    } else if (!DIAG && !failed && sb < chunk_end) {
       // ------------------------------------------ TPW 16-row tiles of one superblock
       uint4 q0[TPW][2], q1[TPW][2];
       uint32_t A_min[TPW][2];
@@ -492,6 +612,15 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     ++cstep;
     // ------------------------------------------------ end of a unit
     if (++cw.g == cw.ge) {
+      if constexpr (DIAG) {  // quad thread tig summed its own sub-blocks only
+#pragma unroll
+        for (int t = 0; t < TPW; ++t)
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            acc[t][0][r] += __shfl_xor_sync(0xffffffffu, acc[t][0][r], 1);
+            acc[t][0][r] += __shfl_xor_sync(0xffffffffu, acc[t][0][r], 2);
+          }
+      }
       constexpr int PER_LANE = TPW * NT * 2;
       float* slot = red + (size_t)((nunit & 1) * WARPS + warp) * 32 * PER_LANE + lane * PER_LANE;
 #pragma unroll
@@ -585,11 +714,11 @@ constexpr size_t gemv_smem() {
          (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
 }
 
-template <bool GATEUP, int NT>
+template <bool GATEUP, int NT, bool DIAG = false>
 cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                         cudaStream_t s) {
   using S = Shape<GATEUP, NT>;
-  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES, S::CPS>;
+  auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES, S::CPS, DIAG>;
   constexpr size_t smem = gemv_smem<GATEUP, NT>();
   static uint64_t attr_set = 0;  // one bit per device
   const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
@@ -602,7 +731,8 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
 template <bool GATEUP>
 cudaError_t launch_gemv_nt(int nt, const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                            cudaStream_t s) {
-  return nt == 1   ? launch_gemv<GATEUP, 1>(t0, t1, P, grid, s)
+  return P.diag ? launch_gemv<GATEUP, 1, true>(t0, t1, P, grid, s)
+         : nt == 1 ? launch_gemv<GATEUP, 1>(t0, t1, P, grid, s)
          : nt == 2 ? launch_gemv<GATEUP, 2>(t0, t1, P, grid, s)
          : nt == 3 ? launch_gemv<GATEUP, 3>(t0, t1, P, grid, s)
                    : launch_gemv<GATEUP, 4>(t0, t1, P, grid, s);
@@ -666,9 +796,15 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
       !weight_map(&md, wd, p.hidden, nsb2, 16 * cb2, sl2))
     return cudaErrorInvalidValue;
 
+  // One token on the float32 path: block-diagonal operands (see frag_token_diag).
+  const bool diag = p.m == 1 && !q8;
   // K0: not a dependent launch, so it also orders this call after the previous one on the stream
   prof.before(0, s);
-  if (bf16 && q8)
+  if (diag && bf16)
+    prep_x_kernel<__nv_bfloat16, false, true><<<nsb1, 32, 0, s>>>((const __nv_bfloat16*)x, p.hidden, 1, 1, f1);
+  else if (diag)
+    prep_x_kernel<float, false, true><<<nsb1, 32, 0, s>>>((const float*)x, p.hidden, 1, 1, f1);
+  else if (bf16 && q8)
     prep_x_kernel<__nv_bfloat16, true><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
   else if (bf16)
     prep_x_kernel<__nv_bfloat16, false><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
@@ -680,7 +816,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err};
+  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err, diag};
   prof.before(1, s);
   e = launch_gemv_nt<true>(p.nt, mg, mu, g1, p.grid1, s);
   prof.after(1, s);
@@ -693,15 +829,16 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
     uint8_t* hq = q8h;
     float2* hds = q8 ? (float2*)(q8h + (size_t)p.m * p.inter) : nullptr;
     void* args[] = {&pp, &nks, &m, &inter, &nt, &f, &hq, &hds};
-    const void* fn = q8 ? reinterpret_cast<const void*>(finish_gateup_kernel<true>)
-                        : reinterpret_cast<const void*>(finish_gateup_kernel<false>);
+    const void* fn = q8     ? reinterpret_cast<const void*>(finish_gateup_kernel<true>)
+                     : diag ? reinterpret_cast<const void*>(finish_gateup_kernel<false, true>)
+                            : reinterpret_cast<const void*>(finish_gateup_kernel<false>);
     prof.before(2, s);
-    e = launch_pdl(fn, dim3(nsb2), dim3(128 * p.nt), 0, s, args);
+    e = launch_pdl(fn, dim3(nsb2), dim3(diag ? 32 : 128 * p.nt), 0, s, args);
     prof.after(2, s);
     if (e != cudaSuccess) return e;
   }
 
-  GemvParams g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, f2, p2, err};
+  GemvParams g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, f2, p2, err, diag};
   prof.before(3, s);
   e = launch_gemv_nt<false>(p.nt, md, md, g2, p.grid2, s);
   prof.after(3, s);
