@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--no-q8", action="store_true", help="skip the Q8_1-activation decode leg")
     ap.add_argument("--no-q6k", action="store_true", help="skip the Q6_K LM-head GEMV leg")
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny, 13B batched and 8B prefill legs")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer loops")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -612,7 +613,7 @@ def main():
         __graft_entry__.build()
 
     K = max(1, args.steps)
-    r = gpu_decode(cfg, K, args.warmup, rank, world, dist, e2e=True)
+    r = gpu_decode(cfg, K, args.warmup, rank, world, dist, e2e=not args.no_e2e)
     ms, rate = whole_job(r["ms"], r["wbytes"] * r["K"], dist)
     value = rate / 1e9
     pk, pk_kind = peaks()
@@ -640,7 +641,7 @@ def main():
     roof = dict(head["roofline"])
     roof["traffic"] = profiled_traffic("decode_gateup_llama7b_m1.txt", src_hash("decode.cu", "common.cuh"))
     roof["step_frac"] = head["step_frac"]
-    e2e_val = r["wbytes"] * r["E"] / (r["e2e_ms"] * 1e-3) / 1e9
+    e2e_val = r["wbytes"] * r["E"] / (r["e2e_ms"] * 1e-3) / 1e9 if r["E"] else None
     line = {"metric": metric, "value": value, "unit": "GB/s", "n_gpus": world, "steps": r["K"],
             "warmup": args.warmup, "ms_per_step": ms / r["K"],
             "ms_per_step_p10_p50_p90": [r["pct"][10], r["pct"][50], r["pct"][90]],
@@ -655,7 +656,7 @@ def main():
                     "d2h_bytes_per_step": r["xbytes"], "steps": r["E"],
                     "note": "every step: the C-ABI call with x and y in page-locked host memory (the kernels "
                             "read x and write y across NVLink-C2C), then a stream sync",
-                    "with_copies": {"value": r["wbytes"] * r["E"] / (r["e2e_copy_ms"] * 1e-3) / 1e9,
+                    "with_copies": {"value": r["wbytes"] * r["E"] / (r["e2e_copy_ms"] * 1e-3) / 1e9 if r["E"] else None,
                                     "note": "pinned x -> device copy, the call, device y -> pinned host copy, "
                                             "stream sync, every step"}},
             "gpu_launches": r["launches_per_step"] * r["K"] * world,
