@@ -132,11 +132,14 @@ __device__ __forceinline__ void frag_token(const float v_in[8], bool zero, int t
 // 2tig's (or 2tig+1's) partial dot product alone and the 6-bit scale is
 // applied once per superblock in float32. MMA index k: 0..7 = low nibbles of
 // quant bytes 4k..4k+3 of the group, 8..15 = their high nibbles. Layout per
-// superblock: fx [16 MMAs][8 lanes with data: lane 4g + (g >> 1)] uint2 (b0 = x
-// at bytes 0 and 2 of the word, b1 = x at bytes 1 and 3; g = 2tig + part), fm as
-// float [8] sub-block sums of x * 2^-e, sc [1] 2^e. Lane L holds x[8L .. 8L+7]
-// of the superblock: quant group L >> 3, nibble half (L >> 2) & 1, MMAs
-// 2(L & 3) and 2(L & 3) + 1.
+// superblock, one record of DREC bytes at fx + sb * DREC (a multiple of 16, so a
+// group of records is one bulk copy): [16 MMAs][8 lanes with data: lane 4g +
+// (g >> 1)] uint2 (b0 = x at bytes 0 and 2 of the word, b1 = x at bytes 1 and 3;
+// g = 2tig + part), then 8 floats: the sub-block sums of x * 2^-e, then 2^e.
+// Lane L holds x[8L .. 8L+7] of the superblock: quant group L >> 3, nibble half
+// (L >> 2) & 1, MMAs 2(L & 3) and 2(L & 3) + 1.
+constexpr int DREC = 1088;
+constexpr int DREC_X = 1024, DREC_SC = 1056;  // byte offsets of the sums and of 2^e
 __device__ __forceinline__ void frag_token_diag(const float v_in[8], int sb, FragPtrs f) {
   const int lane = threadIdx.x & 31;
   float amax = 0.f;
@@ -157,10 +160,10 @@ __device__ __forceinline__ void frag_token_diag(const float v_in[8], int sb, Fra
   }
   xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);  // lanes 4j .. 4j+3 hold sub-block j
   xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
-  float* X = reinterpret_cast<float*>(f.fm) + (int64_t)sb * 8;
-  if ((lane & 3) == 0) X[lane >> 2] = xsum;
+  uint8_t* rec = reinterpret_cast<uint8_t*>(f.fx) + (int64_t)sb * DREC;
+  if ((lane & 3) == 0) reinterpret_cast<float*>(rec + DREC_X)[lane >> 2] = xsum;
   const int tig = lane >> 3, half = (lane >> 2) & 1, s0 = 2 * (lane & 3);
-  uint2* fx = f.fx + (int64_t)sb * 16 * 8;
+  uint2* fx = reinterpret_cast<uint2*>(rec);
 #pragma unroll
   for (int ss = 0; ss < 2; ++ss) {
     const int k = half * 8 + s0 + ss;
@@ -173,7 +176,7 @@ __device__ __forceinline__ void frag_token_diag(const float v_in[8], int sb, Fra
       fx[k * 8 + 2 * tig + part] = fr;
     }
   }
-  if (lane == 0) f.sc[sb] = __uint_as_float((uint32_t)(127 + e) << 23);
+  if (lane == 0) reinterpret_cast<float*>(rec + DREC_SC)[0] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
 // Loads the 8 inputs of this lane (float32 or bf16, widened exactly).
@@ -304,8 +307,12 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   constexpr int MATS = GATEUP ? 2 : 1;
   constexpr int BOX_BYTES = SLICES * RU * BLK;        // one box: [SLICES][RU rows][144 B]
   constexpr int STAGE_BYTES = MATS * BOX_BYTES;
+  // One token, down projection: each step's superblocks change, so their B records
+  // travel with the weights, one bulk copy per stage behind the boxes.
+  constexpr bool BSMEM = DIAG && !GATEUP;
+  constexpr int STAGE_TOTAL = STAGE_BYTES + (BSMEM ? SLICES * DREC : 0);
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_TOTAL);
   uint64_t* empty = full + STAGES;
   float* red = reinterpret_cast<float*>(empty + STAGES);  // [2][WARPS][32 lanes][TPW][NT][2]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(red + 2 * WARPS * 32 * TPW * NT * 2);
@@ -354,13 +361,28 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   walk_start(pw, u0);
   int pstep = 0;
   const uint64_t pol = policy_evict_first();
-  auto produce = [&]() -> bool {  // issue the next step's loads; false on a timed-out wait
+  // B records of superblock group grp into the stage of step `step` (after the input is ready)
+  auto issue_b = [&](int step, int grp) {
+    const int n = min(SLICES, P.nsb - grp * SLICES);
+    bulk_g2s(smem + (step % STAGES) * STAGE_TOTAL + STAGE_BYTES,
+             reinterpret_cast<const uint8_t*>(P.in.fx) + (int64_t)grp * SLICES * DREC, (uint32_t)(n * DREC),
+             &full[step % STAGES]);
+  };
+  int pre_grp[STAGES];  // groups of the steps issued before the input was ready
+  auto produce = [&](bool input_ready) -> bool {  // issue the next step's loads; false on a timed-out wait
     const int s = pstep % STAGES;
     if (pstep >= STAGES && !mbar_wait(&empty[s], (uint32_t)((pstep / STAGES) - 1) & 1u, P.err)) return false;
-    uint8_t* st = smem + s * STAGE_BYTES;
-    mbar_arrive_expect_tx(&full[s], STAGE_BYTES);
+    uint8_t* st = smem + s * STAGE_TOTAL;
+    const int bbytes = BSMEM ? min(SLICES, P.nsb - pw.g * SLICES) * DREC : 0;
+    mbar_arrive_expect_tx(&full[s], STAGE_BYTES + bbytes);
     tma_box3(st, &tm0, pw.ru * RU, pw.g * SLICES, &full[s], pol);
     if (GATEUP) tma_box3(st + BOX_BYTES, &tm1, pw.ru * RU, pw.g * SLICES, &full[s], pol);
+    if (BSMEM) {
+      if (input_ready)
+        issue_b(pstep, pw.g);
+      else
+        pre_grp[pstep] = pw.g;
+    }
     ++pstep;
     if (++pw.g == pw.ge) walk_next(pw);
     return true;
@@ -368,7 +390,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   bool failed = false;  // warp-uniform once the loop starts
   if (producer) {
     for (int i = 0; i < STAGES - 1 && pw.u < u1; ++i)
-      if (!produce()) {
+      if (!produce(false)) {
         failed = true;
         *abort_flag = 1;
         break;
@@ -377,6 +399,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   failed = __any_sync(0xffffffffu, failed);
   pdl_launch_dependents();
   pdl_wait();  // input fragments come from the previous kernel
+  if (BSMEM && producer)
+    for (int i = 0; i < pstep; ++i) issue_b(i, pre_grp[i]);
 
   // B fragment lane to read for token tile n: this lane when its token is real,
   // else the same position of token 4n (always real); the columns of padding
@@ -423,7 +447,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 #pragma unroll 1
   while (cw.u < u1) {
     bool pf = false;
-    if (producer && !failed && pw.u < u1) pf = !produce();
+    if (producer && !failed && pw.u < u1) pf = !produce(true);
     if (__any_sync(0xffffffffu, pf)) {
       failed = true;
       *abort_flag = 1;
@@ -442,22 +466,23 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
     const int chunk_end = min(P.nsb, (cw.ks + 1) * P.gpc * SLICES);
     if (DIAG && !failed && sb < chunk_end) {
       // ------------------------------------------ TPW 16-row tiles of one superblock, one token
-      if (sb != csb) {
-        const uint2* fxd = P.in.fx + (int64_t)sb * 16 * 8;
-        const bool act = (g >> 1) == tig;  // this lane's B column pair belongs to its own quant group
+      const bool act = (g >> 1) == tig;  // this lane's B column pair belongs to its own quant group
+      if (BSMEM || sb != csb) {
+        const uint8_t* rec = BSMEM ? smem + s * STAGE_TOTAL + STAGE_BYTES + slice * DREC
+                                   : reinterpret_cast<const uint8_t*>(P.in.fx) + (int64_t)sb * DREC;
+        const uint2* fxd = reinterpret_cast<const uint2*>(rec);
 #pragma unroll
         for (int k = 0; k < 16; ++k) bc[k][0] = act ? fxd[k * 8 + g] : make_uint2(0u, 0u);
-        const float* X = reinterpret_cast<const float*>(P.in.fm) + (int64_t)sb * 8;
-        xlo = X[2 * tig];
-        xhi = X[2 * tig + 1];
-        xsc[0] = P.in.sc[sb] * 1048576.f;  // 2^e * 2^20
+        xlo = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig];
+        xhi = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig + 1];
+        xsc[0] = reinterpret_cast<const float*>(rec + DREC_SC)[0] * 1048576.f;  // 2^e * 2^20
         csb = sb;
       }
 #pragma unroll
       for (int t = 0; t < TPW; ++t) {
         const int cb = tgrp * TPW + t;
-        const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
-                                                                 : (slice * RU + cb * ROWS) * BLK);
+        const uint8_t* base = smem + s * STAGE_TOTAL + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
+                                                                  : (slice * RU + cb * ROWS) * BLK);
         uint4 hd[2], q0[2], q1[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -506,8 +531,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
 #pragma unroll
       for (int t = 0; t < TPW; ++t) {
         const int cb = tgrp * TPW + t;
-        const uint8_t* base = smem + s * STAGE_BYTES + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
-                                                                 : (slice * RU + cb * ROWS) * BLK);
+        const uint8_t* base = smem + s * STAGE_TOTAL + (GATEUP ? cb * BOX_BYTES + slice * RU * BLK
+                                                                  : (slice * RU + cb * ROWS) * BLK);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const uint8_t* rb = base + (g + 8 * r) * BLK;
@@ -707,11 +732,11 @@ template <bool GATEUP>
 cudaError_t launch_gemv_nt(int nt, const CUtensorMap& t0, const CUtensorMap& t1, const GemvParams& P, int grid,
                            cudaStream_t s);
 
-template <bool GATEUP, int NT>
+template <bool GATEUP, int NT, bool DIAG>
 constexpr size_t gemv_smem() {
   using S = Shape<GATEUP, NT>;
-  return (size_t)S::STAGES * S::COMBOS * 16 * S::SLICES * BLK + 2 * S::STAGES * 8 +
-         (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
+  constexpr size_t stage = (size_t)S::COMBOS * 16 * S::SLICES * BLK + (DIAG && !GATEUP ? (size_t)S::SLICES * DREC : 0);
+  return S::STAGES * stage + 2 * S::STAGES * 8 + (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
 }
 
 template <bool GATEUP, int NT, bool DIAG = false>
@@ -719,7 +744,7 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
                         cudaStream_t s) {
   using S = Shape<GATEUP, NT>;
   auto kern = gemv_kernel<GATEUP, NT, S::COMBOS, S::TPW, S::SLICES, S::STAGES, S::CPS, DIAG>;
-  constexpr size_t smem = gemv_smem<GATEUP, NT>();
+  constexpr size_t smem = gemv_smem<GATEUP, NT, DIAG>();
   static uint64_t attr_set = 0;  // one bit per device
   const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
   if (e != cudaSuccess) return e;
