@@ -469,6 +469,37 @@ def gpu_prefill(cfg, steps, world):
             "launches_per_step": launches, "timed_s": t1 - t0}
 
 
+def gpu_fp8_gemm(cfg, reps=20):
+    """The FP8 tensor-path Q4_K x Q8_1 GEMM (tcgen05 kind::f8f6f4) on the gate projection of `cfg`:
+    Q8_1 activations [m, hidden] x W_gate [inter rows] -> [m, inter] float32; CUDA events over `reps`
+    back-to-back calls (two kernels each: operand planes, GEMM) and around the GEMM kernel alone."""
+    import numpy as np
+    import torch
+    import workloads
+    import q4_swiglu_ffn_gb300 as q
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m, k, n = cfg.m, cfg.hidden, cfg.inter
+    wg = torch.from_numpy(workloads.weights(cfg)[0]).to(dev)
+    xf, _ = workloads.activations(cfg)
+    xq8 = torch.empty(q.q8_1_bytes(m, k), dtype=torch.uint8, device=dev)
+    q.q8_1_quantize_act(torch.from_numpy(xf).to(dev), xq8)
+    ws = torch.empty(q.q4k_mmq_fp8_workspace_bytes(m, k), dtype=torch.uint8, device=dev)
+    out = torch.empty((m, n), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        q.q4k_mmq_fp8(xq8, m, k, wg, workspace=ws, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = _events(2)
+    e0.record()
+    for _ in range(reps):
+        q.q4k_mmq_fp8(xq8, m, k, wg, workspace=ws, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    assert q.q4k_check_device_error() == 0
+    ops = 2 * m * k * n
+    return {"cfg": cfg, "ms": ms, "ops": ops, "reps": reps}
+
+
 def gpu_int8_peak(world):
     """The int8 tensor rate of this part (mma.sync m16n8k32 s8), measured now: best of 5 launches."""
     import torch
@@ -631,6 +662,7 @@ def main():
         if not args.no_configs:
             pre["prefill_8b_h4096_i14336_m512"] = gpu_prefill(workloads.PREFILL_8B, 4 * args.prefill_steps, 1)
         pre["prefill_27b_h5120_i17408_m2048"] = gpu_prefill(workloads.LONG_PREFILL_27B, args.prefill_steps, 1)
+    f8 = gpu_fp8_gemm(workloads.LONG_PREFILL_27B) if (lead and not args.no_prefill) else None
     cb = cpu_baseline(args.cpu_budget_s) if (lead and world == 1) else None
 
     if not lead:
@@ -687,6 +719,22 @@ def main():
         line["int8_tensor_peak"] = int8
     for key, p in pre.items():
         line[key] = prefill_object(p, pk, pk_kind, int8)
+    if f8 is not None:
+        c = f8["cfg"]
+        ach = f8["ops"] / (f8["ms"] * 1e-3) / 1e12
+        fp8_peak = 2.0 * pk["bf16_tflops"]
+        o = {"workload": f"{c.name} gate projection only (m {c.m}, k {c.hidden}, n {c.inter})",
+             "value": ach, "unit": "TOPS (int8-equivalent)", "ms_per_call": f8["ms"], "calls": f8["reps"],
+             "dtype": "e4m3 x e4m3 tcgen05 kind::f8f6f4, exact integer products, f32 scales per sub-block",
+             "roofline": {"kernel": "mmq_fp8_kernel (tcgen05 kind::f8f6f4)", "bound": "tensor", "achieved": ach,
+                          "peak": fp8_peak, "unit": "TFLOP/s", "frac": ach / fp8_peak,
+                          "peak_kind": f"{pk_kind} burst dense bf16 x 2 (the nominal fp8/bf16 ratio)",
+                          "note": "the call includes the operand-plane kernel; per op it executes 2 MMAs (hi, lo)"}}
+        gp = pre.get("prefill_27b_h5120_i17408_m2048")
+        if gp is not None:
+            gu_ops = 2 * c.m * c.hidden * c.inter * 2
+            o["fp16_mmq_gate_up_tops_same_run"] = gu_ops / (gp["kern_ms"][2] * 1e-3) / 1e12
+        line["prefill_fp8_gemm_prototype"] = o
     print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

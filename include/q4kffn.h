@@ -260,6 +260,25 @@ q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream);
  * whole call leave the hook off. */
 q4k_status q4k_set_profile_events(void* const* events, int n);
 
+/* Q4_K x Q8_1 GEMM with FP8 tensor-core operands (tcgen05 kind::f8f6f4, E4M3 x
+ * E4M3, exact integer products): out[t][r] = sum_k deq(W)[r][k] * deq(xq)[t][k]
+ * for t < m tokens and r < n rows. Source: spark_model/layers/ops/q4k_mmq.rs,
+ * q4k_mmq_gemm (C[m, n] = A_q8[m, k] x W_q4k[n, k]^T, activations quantized to
+ * Q8_1 before the GEMM). The 4-bit quants enter the MMA unscaled as E4M3 codes
+ * (exact), each Q8_1 quant as 16*h + l with both parts exact in E4M3, and one
+ * MMA of K = 32 forms one sub-block's integer dot product exactly; the 6-bit
+ * scales, the Q8_1 scales and the min terms are applied in float32 per
+ * sub-block. xq8: planar Q8_1 of the activations [m][k] (q8_1_bytes(m, k)
+ * bytes, as written by q8_1_quantize_act); W: n rows of k/256 Q4_K blocks
+ * (row = output); out float32 [m][n]. k a multiple of 256, n a multiple of
+ * 128, m >= 1 (else Q4K_ERR_SHAPE). Workspace: caller-owned, 256-byte aligned,
+ * q4k_mmq_fp8_workspace_bytes(m, k) bytes (the two E4M3 planes of the
+ * activations), no initialisation needed. Launches two kernels on `stream`. */
+q4k_status q4k_mmq_fp8(const void* xq8, int64_t m, int64_t k, const void* W, int64_t n, float* out,
+                       void* workspace, size_t ws_bytes, q4k_stream_t stream);
+/* Workspace bytes q4k_mmq_fp8 needs (0 for an invalid shape). */
+size_t q4k_mmq_fp8_workspace_bytes(int64_t m, int64_t k);
+
 /* Benchmark hook (no counterpart on the source pages): the int8 tensor-core
  * rate. Enqueues on `stream` one kernel in which every warp issues `iters`
  * rounds of 8 independent mma.sync.m16n8k32 s8 x s8 -> s32 operations (the

@@ -51,6 +51,8 @@ _SIGS = {
     "q4k_last_call_kernels": (_int, []),
     "q4k_status_string": (ctypes.c_char_p, [_int]),
     "q4k_bench_int8_mma": (_int, [_i64, ctypes.POINTER(ctypes.c_double), _p]),
+    "q4k_mmq_fp8": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
+    "q4k_mmq_fp8_workspace_bytes": (_sz, [_i64, _i64]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -248,6 +250,24 @@ _prof_keep = None
 def q4k_last_call_kernels() -> int:
     """Kernels the last FFN or Q6_K GEMV call on this thread launched (benchmark hook)."""
     return lib.q4k_last_call_kernels()
+
+
+def q4k_mmq_fp8_workspace_bytes(m: int, k: int) -> int:
+    return lib.q4k_mmq_fp8_workspace_bytes(m, k)
+
+
+def q4k_mmq_fp8(xq8, m, k, W, workspace=None, out=None, stream=None):
+    """Q4_K x Q8_1 GEMM on the FP8 tensor path: xq8 planar Q8_1 bytes of [m, k] activations,
+    W Q4_K bytes [n, k/256, 144] -> out float32 [m, n] (out[t][r] = sum_k W[r][k] x[t][k])."""
+    import torch
+    n = W.shape[0]
+    if workspace is None:
+        workspace = torch.empty(q4k_mmq_fp8_workspace_bytes(m, k), dtype=torch.uint8, device=W.device)
+    if out is None:
+        out = torch.empty((m, n), dtype=torch.float32, device=W.device)
+    _check(lib.q4k_mmq_fp8(_ptr(xq8), m, k, _ptr(W), n, _ptr(out), _ptr(workspace), workspace.numel(),
+                           _stream(stream)), "q4k_mmq_fp8")
+    return out
 
 
 def q4k_bench_int8_mma(iters: int, stream=None) -> float:
