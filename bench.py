@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--no-q6k", action="store_true", help="skip the Q6_K LM-head GEMV leg")
     ap.add_argument("--no-configs", action="store_true", help="skip the tiny, 13B batched and 8B prefill legs")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end host-buffer loops")
+    ap.add_argument("--quick", action="store_true",
+                    help="short counts everywhere (no clock lead-in, 64-step secondary legs, 20 profiled calls): "
+                         "for launch-list captures")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
 
@@ -262,10 +265,14 @@ def _events(n):
     return ev
 
 
+QUICK = False
+
+
 def _kernel_ms(q, step, P: int, nk: int):
     """Mean duration of each of the call's kernels over P calls (events around each kernel;
     they serialise the kernels, so these are per-kernel, not per-call, figures)."""
     import torch
+    P = min(P, 20) if QUICK else P
     evs = [_events(2 * nk) for _ in range(P)]
     torch.cuda.synchronize()
     for i in range(P):
@@ -320,7 +327,7 @@ def gpu_decode(cfg, K, warmup, rank, world, dist, path="f32", e2e=False):
     sampler = ClockSampler(_gpu_index(dev, world))
     time.sleep(0.3)
     # a long untimed lead-in keeps the clocks at their loaded value into the timed region
-    lead = Steps(step, max(K, 2000), R, stream) if K < 2000 else runs
+    lead = Steps(step, max(K, 2000), R, stream) if (K < 2000 and not QUICK) else runs
     ev = _events(runs.full + 2)
     if dist:
         dist.barrier()
@@ -338,7 +345,7 @@ def gpu_decode(cfg, K, warmup, rank, world, dist, path="f32", e2e=False):
     pct = {p: per_step[min(n - 1, int(p / 100 * n))] for p in (10, 50, 90)}
     # a longer timed run beside the K steps: many steps, so the spread and clocks mean something
     long_ms, long_K = None, 0
-    if K < 2000:
+    if lead is not runs:
         ev2 = _events(lead.full + 2)
         lead.replay_all(ev2)
         torch.cuda.synchronize()
@@ -505,7 +512,7 @@ def gpu_int8_peak(world):
     import torch
     import q4_swiglu_ffn_gb300 as q
     dev = torch.device("cuda", torch.cuda.current_device())
-    iters = 8192
+    iters = 512 if QUICK else 8192
     for _ in range(2):
         q.q4k_bench_int8_mma(iters)
     torch.cuda.synchronize()
@@ -599,7 +606,10 @@ def prefill_object(pre, pk, pk_kind, int8):
 
 
 def main():
+    global QUICK
     args = parse()
+    QUICK = args.quick
+    legK = 64 if QUICK else 2000
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -650,19 +660,21 @@ def main():
     pk, pk_kind = peaks()
     lead = rank == 0
 
-    r8 = gpu_decode(cfg, 2000, 3, rank, 1, None, path="q8_1") if (lead and not args.no_q8) else None
-    r6 = gpu_q6k(1000) if (lead and not args.no_q6k) else None
+    r8 = gpu_decode(cfg, legK, 3, rank, 1, None, path="q8_1") if (lead and not args.no_q8) else None
+    r6 = gpu_q6k(legK // 2) if (lead and not args.no_q6k) else None
     others = {}
     if lead and not args.no_configs:
-        others["decode_tiny_h256_i768_m1"] = gpu_decode(workloads.TINY_DECODE, 2000, 3, rank, 1, None)
-        others["decode_13b_h5120_i13824_m8"] = gpu_decode(workloads.BATCHED_13B_DECODE, 2000, 3, rank, 1, None)
+        others["decode_tiny_h256_i768_m1"] = gpu_decode(workloads.TINY_DECODE, legK, 3, rank, 1, None)
+        others["decode_13b_h5120_i13824_m8"] = gpu_decode(workloads.BATCHED_13B_DECODE, legK, 3, rank, 1, None)
     int8 = gpu_int8_peak(1) if (lead and not args.no_prefill) else None
     pre = {}
     if lead and not args.no_prefill:
         if not args.no_configs:
-            pre["prefill_8b_h4096_i14336_m512"] = gpu_prefill(workloads.PREFILL_8B, 4 * args.prefill_steps, 1)
-        pre["prefill_27b_h5120_i17408_m2048"] = gpu_prefill(workloads.LONG_PREFILL_27B, args.prefill_steps, 1)
-    f8 = gpu_fp8_gemm(workloads.LONG_PREFILL_27B) if (lead and not args.no_prefill) else None
+            pre["prefill_8b_h4096_i14336_m512"] = gpu_prefill(workloads.PREFILL_8B,
+                                                              (4 if QUICK else 4 * args.prefill_steps), 1)
+        pre["prefill_27b_h5120_i17408_m2048"] = gpu_prefill(workloads.LONG_PREFILL_27B,
+                                                              (4 if QUICK else args.prefill_steps), 1)
+    f8 = gpu_fp8_gemm(workloads.LONG_PREFILL_27B, 4 if QUICK else 20) if (lead and not args.no_prefill) else None
     cb = cpu_baseline(args.cpu_budget_s) if (lead and world == 1) else None
 
     if not lead:
