@@ -554,13 +554,15 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           A_min[t][r] = h2_as_u32(__hsub2(u32_as_h2(mnb), u32_as_h2(0x64006400u)));
         }
       }
-      float c[TPW][NT][2][4], cm[TPW][NT][4];
+      // Low-nibble (sub-block 2tig) and high-nibble (2tig+1) weights both enter as
+      // exact q * scale, so one accumulator per tile and token tile takes both.
+      float c[TPW][NT][4], cm[TPW][NT][4];
 #pragma unroll
       for (int t = 0; t < TPW; ++t)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) c[t][n][0][i] = c[t][n][1][i] = cm[t][n][i] = 0.f;
+          for (int i = 0; i < 4; ++i) c[t][n][i] = cm[t][n][i] = 0.f;
       const uint2* fx = P.in.fx + (int64_t)sb * 16 * NT * 32;
       if (sb != csb) {
         if constexpr (CACHEB) {
@@ -604,8 +606,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           }
 #pragma unroll
           for (int n = 0; n < NT; ++n) {
-            mma16816(c[t][n][0], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
-            mma16816(c[t][n][1], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
+            mma16816(c[t][n], L0[0], L0[1], L1[0], L1[1], b0[n].x, b0[n].y);
+            mma16816(c[t][n], H0[0], H0[1], H1[0], H1[1], b1[n].x, b1[n].y);
           }
         }
       }
@@ -624,8 +626,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
         for (int t = 0; t < TPW; ++t)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            const float main =
-                (c[t][n][0][2 * r] + c[t][n][1][2 * r]) + (c[t][n][0][2 * r + 1] + c[t][n][1][2 * r + 1]);
+            const float main = c[t][n][2 * r] + c[t][n][2 * r + 1];
             const float mins = cm[t][n][2 * r] + cm[t][n][2 * r + 1];
             acc[t][n][r] = fmaf(main, dd[t][r] * xs, acc[t][n][r]);
             acc[t][n][r] = fmaf(-mins, dm[t][r] * (64.f * xs), acc[t][n][r]);
