@@ -75,20 +75,38 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
+_current_raw_stream = None  # () -> the current device's current CUDA stream, as a raw handle
+
+
 def _stream(stream):
-    import torch
+    """The stream argument as a raw handle; None is PyTorch's current stream."""
+    global _current_raw_stream
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if _current_raw_stream is None:
+            import torch
+            get_raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            get_dev = getattr(torch._C, "_cuda_getDevice", None)
+            if get_raw is not None and get_dev is not None:
+                torch.cuda.init()
+                _current_raw_stream = lambda: get_raw(get_dev())
+            else:  # same handle through the public API (slower: builds a Stream object)
+                _current_raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+        return _current_raw_stream()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+_DTYPES = None  # {torch.float32: Q4K_F32, torch.bfloat16: Q4K_BF16}
+
+
 def _dtype_code(t) -> int:
-    import torch
-    if t.dtype == torch.float32:
-        return Q4K_F32
-    if t.dtype == torch.bfloat16:
-        return Q4K_BF16
-    raise TypeError(f"unsupported activation dtype {t.dtype}")
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+        _DTYPES = {torch.float32: Q4K_F32, torch.bfloat16: Q4K_BF16}
+    code = _DTYPES.get(t.dtype)
+    if code is None:
+        raise TypeError(f"unsupported activation dtype {t.dtype}")
+    return code
 
 
 def q4k_weight_bytes(rows: int, cols: int) -> int:
@@ -138,10 +156,10 @@ def q8_1_quantize_act(x, out=None, stream=None):
 
 def ffn_q4k_swiglu(x, W_gate, W_up, W_down, y=None, stream=None):
     """y = W_down (silu(W_gate x) * (W_up x)); x float32 [m, hidden] -> y float32 [m, hidden]."""
-    import torch
     m, hidden = x.shape
     inter = W_gate.shape[0]
     if y is None:
+        import torch
         y = torch.empty((m, hidden), dtype=torch.float32, device=x.device)
     _check(lib.ffn_q4k_swiglu(_ptr(x), m, hidden, inter, _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(y),
                               _stream(stream)), "ffn_q4k_swiglu")
@@ -149,7 +167,7 @@ def ffn_q4k_swiglu(x, W_gate, W_up, W_down, y=None, stream=None):
 
 
 def ffn_q4k_swiglu_ex(x, W_gate, W_up, W_down, workspace, y=None, stream=None):
-    """As ffn_q4k_swiglu with float32 or bf16 x and a caller workspace (uint8 CUDA tensor, zeroed once)."""
+    """As ffn_q4k_swiglu with float32 or bf16 x and a caller workspace (uint8 CUDA tensor; any contents)."""
     import torch
     m, hidden = x.shape
     inter = W_gate.shape[0]

@@ -129,3 +129,13 @@ def test_decode_passes_of_16_tokens(m):
     ref, _ = oracle.ffn_decode(x, wg, wu, wd)
     check_close(y, ref, TIGHT_L2, TIGHT_MAX)
     assert lib().ffn_q4k_workspace_h_q8_1_offset(m, 1024, 1536) == 0
+
+
+def test_binding_enqueues_on_the_current_stream():
+    """Without a stream argument the binding uses PyTorch's current stream of the current device."""
+    q = lib()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert q._stream(None) == s.cuda_stream == torch.cuda.current_stream().cuda_stream
+    assert q._stream(None) == torch.cuda.current_stream().cuda_stream
+    assert q._stream(s) == s.cuda_stream
