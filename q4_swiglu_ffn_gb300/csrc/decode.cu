@@ -224,7 +224,14 @@ __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt
     frag_token(v, t >= m, t, nt, sb, f);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
+// and t / (1 + t) below. Nothing overflows, the divisor is in [1, 2] (where __fdividef
+// is within 2 ulp), and there is no branch: the IEEE division's slow path had serialised
+// the 8 values of a lane and made this the longest step of the SwiGLU kernel.
+__device__ __forceinline__ float silu_f(float z) {
+  const float t = expf(-fabsf(z));  // in (0, 1]
+  return z * __fdividef(z >= 0.f ? 1.0f : t, 1.0f + t);
+}
 
 // K1b: one CTA per 256-row block of h, one warp per token slot. Sums the
 // gate/up chunks in order, applies SwiGLU and writes the fragments of h (Q8: of

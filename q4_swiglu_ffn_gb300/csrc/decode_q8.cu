@@ -404,7 +404,14 @@ void shape_q8(int mt, int* combos, int* slices, int* cps) {
     get(ShapeQ8<GATEUP, 2>{});
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
+// and t / (1 + t) below. Nothing overflows, the divisor is in [1, 2] (where __fdividef
+// is within 2 ulp), and there is no branch: the IEEE division's slow path had serialised
+// the 8 values of a lane and made this the longest step of the SwiGLU kernel.
+__device__ __forceinline__ float silu_f(float z) {
+  const float t = expf(-fabsf(z));  // in (0, 1]
+  return z * __fdividef(z >= 0.f ? 1.0f : t, 1.0f + t);
+}
 
 __device__ __forceinline__ void load8f(const float* p, float v[8]) {
   const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];

@@ -169,12 +169,13 @@ struct MmqParams {
 
 constexpr uint32_t IDESC = idesc_f16(TM, TN);
 
-// silu(z) = z / (1 + e^-z). Below z = -80, e^-z > 5.5e34 and the quotient is z * e^z
-// to within 1e-35 relative. Above, the divisor is below 2^126, where CUDA's __fdividef
-// is within 2 ulp and has no branch (the IEEE division's slow-path branch kept the
-// 32 independent values of an item from overlapping).
+// silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
+// and t / (1 + t) below. Nothing overflows, the divisor is in [1, 2], where CUDA's
+// __fdividef is within 2 ulp, and there is no branch (the IEEE division's slow-path
+// branch kept the 32 independent values of an item from overlapping).
 __device__ __forceinline__ float silu_f(float z) {
-  return z < -80.f ? z * expf(z) : __fdividef(z, 1.0f + expf(-z));
+  const float t = expf(-fabsf(z));  // in (0, 1]
+  return z * __fdividef(z >= 0.f ? 1.0f : t, 1.0f + t);
 }
 
 // SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7).
