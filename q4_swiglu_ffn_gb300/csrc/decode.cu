@@ -248,13 +248,21 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
     float g[8], u[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) g[i] = u[i] = 0.f;
-#pragma unroll 4
-    for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
-      float a[8], b[8];
-      load8(part + (((int64_t)k * 2 + 0) * m + t) * inter + i0, a);
-      load8(part + (((int64_t)k * 2 + 1) * m + t) * inter + i0, b);
+    // Batches of 4 chunks: all of a batch's loads are issued before the first add (a
+    // loop over a run-time count would wait for each load in turn); sums in chunk order.
+    for (int k0 = 0; k0 < nks; k0 += 4) {
+      float a[4][8], b[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) g[i] += a[i], u[i] += b[i];
+      for (int j = 0; j < 4; ++j)
+        if (k0 + j < nks) {
+          load8(part + (((int64_t)(k0 + j) * 2 + 0) * m + t) * inter + i0, a[j]);
+          load8(part + (((int64_t)(k0 + j) * 2 + 1) * m + t) * inter + i0, b[j]);
+        }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (k0 + j < nks)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) g[i] += a[j][i], u[i] += b[j][i];
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = silu_f(g[i]) * u[i];

@@ -430,13 +430,21 @@ __global__ void finish_gateup_q8_kernel(const float* __restrict__ part, int nks,
   float g[8], u[8], v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) g[j] = u[j] = 0.f;
-#pragma unroll 4
-  for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
-    float a[8], b[8];
-    load8f(part + (((int64_t)k * 2 + 0) * m + t) * inter + c, a);
-    load8f(part + (((int64_t)k * 2 + 1) * m + t) * inter + c, b);
+  // Batches of 4 chunks: all of a batch's loads are issued before the first add (a loop
+  // over a run-time count would wait for each load in turn); sums in chunk order.
+  for (int k0 = 0; k0 < nks; k0 += 4) {
+    float a[4][8], b[4][8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) g[j] += a[j], u[j] += b[j];
+    for (int jj = 0; jj < 4; ++jj)
+      if (k0 + jj < nks) {
+        load8f(part + (((int64_t)(k0 + jj) * 2 + 0) * m + t) * inter + c, a[jj]);
+        load8f(part + (((int64_t)(k0 + jj) * 2 + 1) * m + t) * inter + c, b[jj]);
+      }
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+      if (k0 + jj < nks)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] += a[jj][j], u[j] += b[jj][j];
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) v[j] = silu_f(g[j]) * u[j];

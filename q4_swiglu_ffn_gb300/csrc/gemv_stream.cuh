@@ -41,10 +41,16 @@ __global__ void finish_down_kernel(const float* __restrict__ part, int nks, int6
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (4 * i >= n) return;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int k = 0; k < nks; ++k) {  // unrolled so that several chunks' loads are in flight
-    const float4 a = reinterpret_cast<const float4*>(part + (int64_t)k * n)[i];
-    s.x += a.x, s.y += a.y, s.z += a.z, s.w += a.w;
+  // Batches of 8 chunks: all of a batch's loads are issued before the first add (a
+  // loop over a run-time count would wait for each load in turn); sums in chunk order.
+  for (int k0 = 0; k0 < nks; k0 += 8) {
+    float4 a[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (k0 + j < nks) a[j] = reinterpret_cast<const float4*>(part + (int64_t)(k0 + j) * n)[i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (k0 + j < nks) s.x += a[j].x, s.y += a[j].y, s.z += a[j].z, s.w += a[j].w;
   }
   store4(y, i, s);
 }

@@ -539,13 +539,15 @@ __global__ void __launch_bounds__(TM) finish_tail_kernel(const float* __restrict
   const int tile = whole + tl, nmt = tiles / ntn;
   const int nt = mt_fast ? tile / nmt : tile % ntn, mt = mt_fast ? tile % nmt : tile / ntn;
   const int r = threadIdx.x;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int q = 0; q < tail_q; ++q)  // the 8 tokens' loads of a slice are in flight together
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (nt * TN + t8 * 8 + i < m) v[i] += tail[(((int64_t)q * ntail + tl) * TN + t8 * 8 + i) * TM + r];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const int tt = t8 * 8 + i, t = nt * TN + tt;
-    if (t >= m) break;
-    float v = 0.f;
-    for (int q = 0; q < tail_q; ++q) v += tail[(((int64_t)q * ntail + tl) * TN + tt) * TM + r];
-    y[(int64_t)t * ldo + mt * TM + r] = v;
+    const int t = nt * TN + t8 * 8 + i;
+    if (t < m) y[(int64_t)t * ldo + mt * TM + r] = v[i];
   }
 }
 
