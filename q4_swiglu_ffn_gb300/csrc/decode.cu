@@ -285,6 +285,13 @@ __global__ void finish_gateup_kernel(const float* __restrict__ part, int nks, in
     frag_token(v, t >= m, t, nt, sb, f);
 }
 
+// Bytes of one stage: the weight boxes, then (one token, down projection) the input
+// records, rounded up so that every stage's first box starts on a 128-byte boundary
+// (the destination alignment of a tensor copy into shared memory).
+__host__ __device__ constexpr int stage_total(int box_bytes, int rec_bytes) {
+  return (box_bytes + rec_bytes + 127) / 128 * 128;
+}
+
 struct GemvParams {
   int rows;           // output rows of each matrix
   int nsb;            // superblocks along K
@@ -325,7 +332,8 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   // One token, down projection: each step's superblocks change, so their B records
   // travel with the weights, one bulk copy per stage behind the boxes.
   constexpr bool BSMEM = DIAG && !GATEUP;
-  constexpr int STAGE_TOTAL = STAGE_BYTES + (BSMEM ? SLICES * DREC : 0);
+  constexpr int STAGE_TOTAL = stage_total(STAGE_BYTES, BSMEM ? SLICES * DREC : 0);
+  static_assert(BOX_BYTES % 128 == 0 && STAGE_TOTAL % 128 == 0, "TMA boxes land on 128-byte boundaries");
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_TOTAL);
   uint64_t* empty = full + STAGES;
@@ -751,7 +759,7 @@ cudaError_t launch_gemv_nt(int nt, const CUtensorMap& t0, const CUtensorMap& t1,
 template <bool GATEUP, int NT, bool DIAG>
 constexpr size_t gemv_smem() {
   using S = Shape<GATEUP, NT>;
-  constexpr size_t stage = (size_t)S::COMBOS * 16 * S::SLICES * BLK + (DIAG && !GATEUP ? (size_t)S::SLICES * DREC : 0);
+  constexpr size_t stage = stage_total(S::COMBOS * 16 * S::SLICES * BLK, DIAG && !GATEUP ? S::SLICES * DREC : 0);
   return S::STAGES * stage + 2 * S::STAGES * 8 + (size_t)2 * S::COMBOS * S::SLICES * 32 * NT * 2 * 4 + 16;
 }
 
