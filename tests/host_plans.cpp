@@ -55,6 +55,12 @@ void check_decode(int sms) {
               "noalloc m %d h %d i %d: %zu bytes", m, h, i, p.ws_bytes);
       }
   q4k::DecodePlan p;
+  // the GPU tests' many-chunk shapes (152 SMs): 8 gate/up chunks, 16 down chunks
+  if (sms == 152) {
+    CHECK(q4k::decode_plan(1, 16384, 256, sms, &p) && p.nks1 == 8, "m 1 h 16384 i 256 nks1 %d", p.nks1);
+    CHECK(q4k::decode_plan(3, 16384, 256, sms, &p) && p.nks1 == 8, "m 3 h 16384 i 256 nks1 %d", p.nks1);
+    CHECK(q4k::decode_plan(2, 256, 32768, sms, &p) && p.nks2 == 16, "m 2 h 256 i 32768 nks2 %d", p.nks2);
+  }
   CHECK(!q4k::decode_plan(0, 4096, 11008, sms, &p), "m 0");
   CHECK(!q4k::decode_plan(q4k::DECODE_PASS_MAX + 1, 4096, 11008, sms, &p), "m above a pass");
 }

@@ -93,6 +93,33 @@ def test_decode_special_inputs():
     check_close(y, ref, TIGHT_L2, TIGHT_MAX)
 
 
+@pytest.mark.parametrize("row", [0, 1, 2])
+def test_decode_one_token_extreme_inputs(row):
+    """One token (the block-diagonal path and its SwiGLU): activations that drive the gate to
+    magnitudes in the 1e5 range (silu's both tails), to 1e-6, and sparse spikes."""
+    c = workloads.small_config(512, 768, 1)
+    x = np.zeros((1, 512), np.float32)
+    if row == 0:
+        x[0] = workloads.normal(5, 1, 512) * 1e4
+    elif row == 1:
+        x[0] = workloads.normal(5, 2, 512) * 1e-6
+    else:
+        x[0, ::7] = 3.0e5
+    y, ref = _run(c, x=x)
+    assert np.all(np.isfinite(y))
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX, f"one token, input {row}")
+
+
+@pytest.mark.parametrize("H,I,m", [(16384, 256, 1), (16384, 256, 3), (256, 32768, 2)])
+def test_decode_many_k_chunks(H, I, m):
+    """Shapes the planner splits into 8 gate/up K-chunks (hidden 16384, one or three tokens) or
+    16 down K-chunks (inter 32768): the chunk sums take their loads in batches (4 chunks in the
+    SwiGLU kernel, 8 in the down-chunk sum), and every batch boundary is crossed."""
+    c = workloads.small_config(H, I, m, "f32", ("channels", 0.01, 20.0))
+    y, ref = _run(c)
+    check_close(y, ref, TIGHT_L2, TIGHT_MAX, f"h {H} i {I} m {m}")
+
+
 def test_decode_bf16_input_through_ex():
     c = workloads.small_config(768, 1024, 4, "bf16", ("channels", 0.01, 100.0))
     wg, wu, wd = workloads.weights(c)
