@@ -1,12 +1,14 @@
 // Decode regime (m = 1..16 tokens per pass) of the Q4_K SwiGLU FFN on sm_103a.
 //
 //   K0  prep_x:         x [m][hidden] -> B fragments (below); per token and superblock
+//                       (one token: not launched, K1 builds them from x)
 //   K1  gemv<gate/up>:  partial g = Wg.x and u = Wu.x per K-chunk, one pass over both
 //   K1b finish_gateup:  g, u = sum of the chunks; h = silu(g) * u -> B fragments
 //   K2  gemv<down>:     partial y = Wd.h per K-chunk
 //   K3  finish_down:    y = sum of the chunks (only when K is split)
-// All but K0 are launched with programmatic dependent launch: each starts (and
-// streams its first weight tiles) while the previous kernel drains.
+// All but the call's first kernel (K0, or K1 for one token) are launched with
+// programmatic dependent launch: each starts (and streams its first weight tiles)
+// while the previous kernel drains.
 // Source: realizar src/cuda/executor/layers/ffn.rs, fused_ffn_swiglu_gpu
 // (gate and up GEMVs of the same input, SwiGLU, down GEMV, chained on one
 // stream without synchronisation); realizar q4k_gemv_cached_uses.rs,
@@ -194,6 +196,63 @@ __device__ __forceinline__ void load8(const __nv_bfloat16* p, float v[8]) {
   }
 }
 
+// One warp, one token: the block-diagonal B operand of superblock sb of x, straight into this
+// lane's registers (the record frag_token_diag would write, as the gate/up GEMV reads it):
+// bc[k] for MMA k, and the sub-block sums and scale of this lane's quant group. Lane L
+// computes x[8L .. 8L+7] as frag_token_diag does; entry (k, 2p + part) of the record comes
+// from lane 8p + 4(k >> 3) + ((k & 7) >> 1), half k & 1, and lane (g, tig) takes entry
+// (k, g) when g >> 1 == tig (zeros otherwise).
+__device__ __forceinline__ void diag_frags_from_x(const void* x, int xbf16, int sb, uint2 bc[16], float& xlo,
+                                                  float& xhi, float& xsc) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  float v[8];
+  if (xbf16)
+    load8(reinterpret_cast<const __nv_bfloat16*>(x) + (int64_t)sb * QK + lane * 8, v);
+  else
+    load8(reinterpret_cast<const float*>(x) + (int64_t)sb * QK + lane * 8, v);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = warp_max(amax);
+  int e = 0;
+  if (amax > 0.f) e = max((int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 14, -100);
+  const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
+  __half hi[8], lo[8];
+  float xsum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float y = v[i] * s;
+    hi[i] = __float2half_rn(y);
+    lo[i] = __float2half_rn(y - __half2float(hi[i]));
+    xsum += y;
+  }
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 1);  // lanes 4j .. 4j+3 hold sub-block j
+  xsum += __shfl_xor_sync(0xffffffffu, xsum, 2);
+  uint2 E[2][2];  // this lane's entries: [half ss][part (hi, lo)]
+#pragma unroll
+  for (int ss = 0; ss < 2; ++ss)
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+      const __half* h8 = part ? lo : hi;
+      E[ss][part] = make_uint2(h2_as_u32(__halves2half2(h8[4 * ss + 0], h8[4 * ss + 2])),
+                               h2_as_u32(__halves2half2(h8[4 * ss + 1], h8[4 * ss + 3])));
+    }
+  const bool act = (g >> 1) == tig;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const int src = 8 * tig + 4 * (k >> 3) + ((k & 7) >> 1), ss = k & 1;
+    uint2 a0, a1;
+    a0.x = __shfl_sync(0xffffffffu, E[ss][0].x, src);
+    a0.y = __shfl_sync(0xffffffffu, E[ss][0].y, src);
+    a1.x = __shfl_sync(0xffffffffu, E[ss][1].x, src);
+    a1.y = __shfl_sync(0xffffffffu, E[ss][1].y, src);
+    bc[k] = act ? ((g & 1) ? a1 : a0) : make_uint2(0u, 0u);
+  }
+  xlo = __shfl_sync(0xffffffffu, xsum, 8 * tig);
+  xhi = __shfl_sync(0xffffffffu, xsum, 8 * tig + 4);
+  xsc = __uint_as_float((uint32_t)(127 + e) << 23) * 1048576.f;  // 2^e * 2^20
+}
+
 // Q8: x (or h) is first rounded to Q8_1 (blocks of 32 = 4 lanes) and its
 // dequantized values q * d become the B operand, the activations of the Q8_1
 // entry point; the token slot's warp is whole, so the shuffles are safe.
@@ -203,9 +262,9 @@ __device__ __forceinline__ void round_q8_1(float v[8], int8_t q[8], float& d, fl
   for (int i = 0; i < 8; ++i) v[i] = (float)q[i] * d;
 }
 
-// K0: one CTA per superblock of x, one warp per token slot (DIAG: one token,
-// block-diagonal fragments).
-template <typename T, bool Q8, bool DIAG = false>
+// K0: one CTA per superblock of x, one warp per token slot (not launched for one token:
+// the gate/up GEMV builds its block-diagonal fragments itself, diag_frags_from_x).
+template <typename T, bool Q8>
 __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f) {
   pdl_launch_dependents();
   const int t = threadIdx.x >> 5, sb = blockIdx.x, lane = threadIdx.x & 31;
@@ -218,10 +277,7 @@ __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt
       round_q8_1(v, q, d, s);
     }
   }
-  if constexpr (DIAG)
-    frag_token_diag(v, sb, f);
-  else
-    frag_token(v, t >= m, t, nt, sb, f);
+  frag_token(v, t >= m, t, nt, sb, f);
 }
 
 // silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
@@ -302,6 +358,8 @@ struct GemvParams {
   float* out;         // chunk sums: [nks][2][m][rows] (gate/up) or [nks][m][rows] (down)
   uint32_t* err;
   int diag;           // one token with block-diagonal B fragments (frag_token_diag)
+  const void* x;      // one-token gate/up: x itself (the fragments are built in the kernel)
+  int xbf16;          // ... as bf16 (else float32)
 };
 
 __device__ __forceinline__ void mma16816(float c[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -463,6 +521,16 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   float xsc[NT];
   float xlo = 0.f, xhi = 0.f;  // DIAG: sums of x * 2^-e over sub-blocks 2tig and 2tig+1
   int csb = -1;
+  if constexpr (DIAG && GATEUP) {  // x's fragments of the first superblock, while the first weights arrive
+    const int sb0 = cw.g * SLICES + slice;
+    if (cw.u < u1 && sb0 < min(P.nsb, (cw.ks + 1) * P.gpc * SLICES)) {
+      uint2 bt[16];
+      diag_frags_from_x(P.x, P.xbf16, sb0, bt, xlo, xhi, xsc[0]);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) bc[k][0] = bt[k];
+      csb = sb0;
+    }
+  }
 
   // A warp whose wait timed out raises the CTA's abort flag and stops waiting,
   // copying and computing, but still walks its units so that every warp reaches
@@ -491,14 +559,20 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
       // ------------------------------------------ TPW 16-row tiles of one superblock, one token
       const bool act = (g >> 1) == tig;  // this lane's B column pair belongs to its own quant group
       if (BSMEM || sb != csb) {
-        const uint8_t* rec = BSMEM ? smem + s * STAGE_TOTAL + STAGE_BYTES + slice * DREC
-                                   : reinterpret_cast<const uint8_t*>(P.in.fx) + (int64_t)sb * DREC;
-        const uint2* fxd = reinterpret_cast<const uint2*>(rec);
+        if constexpr (BSMEM) {  // h's record, copied into the stage with the weights
+          const uint8_t* rec = smem + s * STAGE_TOTAL + STAGE_BYTES + slice * DREC;
+          const uint2* fxd = reinterpret_cast<const uint2*>(rec);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) bc[k][0] = act ? fxd[k * 8 + g] : make_uint2(0u, 0u);
-        xlo = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig];
-        xhi = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig + 1];
-        xsc[0] = reinterpret_cast<const float*>(rec + DREC_SC)[0] * 1048576.f;  // 2^e * 2^20
+          for (int k = 0; k < 16; ++k) bc[k][0] = act ? fxd[k * 8 + g] : make_uint2(0u, 0u);
+          xlo = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig];
+          xhi = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig + 1];
+          xsc[0] = reinterpret_cast<const float*>(rec + DREC_SC)[0] * 1048576.f;  // 2^e * 2^20
+        } else {  // x's fragments, built here from x (no separate kernel)
+          uint2 bt[16];
+          diag_frags_from_x(P.x, P.xbf16, sb, bt, xlo, xhi, xsc[0]);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) bc[k][0] = bt[k];
+        }
         csb = sb;
       }
 #pragma unroll
@@ -773,8 +847,9 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
   const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<CUtensorMap*>(&t0), const_cast<CUtensorMap*>(&t1), const_cast<GemvParams*>(&P)};
+  // the one-token gate/up GEMV is the call's first kernel (it builds x's fragments itself)
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS / S::TPW * S::SLICES * 32), smem, s,
-                    args);
+                    args, !(GATEUP && DIAG));
 }
 
 template <bool GATEUP>
@@ -827,6 +902,11 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   return true;
 }
 
+int decode_kernels(const DecodePlan& p, bool q8, int ybf16) {
+  const bool diag = p.m == 1 && !q8;  // no K0: K1 builds x's fragments
+  return (diag ? 3 : 4) + (p.nks2 > 1 || ybf16);
+}
+
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
                           void* y, void* ws, uint32_t* err, cudaStream_t s, const ProfileEvents& prof, int ybf16,
                           uint8_t* q8h) {
@@ -845,27 +925,27 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
       !weight_map(&md, wd, p.hidden, nsb2, 16 * cb2, sl2))
     return cudaErrorInvalidValue;
 
-  // One token on the float32 path: block-diagonal operands (see frag_token_diag).
+  // One token on the float32 path: block-diagonal operands (see frag_token_diag). K1 then
+  // builds x's fragments itself and is the call's first kernel (there is no K0).
   const bool diag = p.m == 1 && !q8;
   // K0: not a dependent launch, so it also orders this call after the previous one on the stream
   prof.before(0, s);
-  if (diag && bf16)
-    prep_x_kernel<__nv_bfloat16, false, true><<<nsb1, 32, 0, s>>>((const __nv_bfloat16*)x, p.hidden, 1, 1, f1);
-  else if (diag)
-    prep_x_kernel<float, false, true><<<nsb1, 32, 0, s>>>((const float*)x, p.hidden, 1, 1, f1);
-  else if (bf16 && q8)
-    prep_x_kernel<__nv_bfloat16, true><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
-  else if (bf16)
-    prep_x_kernel<__nv_bfloat16, false><<<nsb1, 128 * p.nt, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
-  else if (q8)
-    prep_x_kernel<float, true><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
-  else
-    prep_x_kernel<float, false><<<nsb1, 128 * p.nt, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
+  if (!diag) {
+    const int nw = 128 * p.nt;  // one warp per token slot
+    if (bf16 && q8)
+      prep_x_kernel<__nv_bfloat16, true><<<nsb1, nw, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
+    else if (bf16)
+      prep_x_kernel<__nv_bfloat16, false><<<nsb1, nw, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
+    else if (q8)
+      prep_x_kernel<float, true><<<nsb1, nw, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
+    else
+      prep_x_kernel<float, false><<<nsb1, nw, 0, s>>>((const float*)x, p.hidden, p.m, p.nt, f1);
+  }
   prof.after(0, s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err, diag};
+  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err, diag, x, bf16};
   prof.before(1, s);
   e = launch_gemv_nt<true>(p.nt, mg, mu, g1, p.grid1, s);
   prof.after(1, s);
@@ -887,7 +967,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
     if (e != cudaSuccess) return e;
   }
 
-  GemvParams g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, f2, p2, err, diag};
+  GemvParams g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, f2, p2, err, diag, nullptr, 0};
   prof.before(3, s);
   e = launch_gemv_nt<false>(p.nt, md, md, g2, p.grid2, s);
   prof.after(3, s);

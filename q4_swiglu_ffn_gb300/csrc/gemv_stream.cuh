@@ -55,7 +55,9 @@ __global__ void finish_down_kernel(const float* __restrict__ part, int nks, int6
   store4(y, i, s);
 }
 
-inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+// pdl = false: an ordinary launch (the first kernel of a call, ordered after all earlier work).
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                              bool pdl = true) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -65,7 +67,7 @@ inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

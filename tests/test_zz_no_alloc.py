@@ -43,7 +43,7 @@ def test_noalloc_matches_the_oracle_twice(cfg_index):
         y = torch.full((m, H), float("nan"), dtype=torch.float32, device=dev())
         st = f(x.data_ptr(), m, H, cfg.inter, wg.data_ptr(), wu.data_ptr(), wd.data_ptr(), y.data_ptr(), stream)
         assert st == 0
-        assert lib().q4k_last_call_kernels() >= 4
+        assert lib().q4k_last_call_kernels() >= (3 if m == 1 else 4)  # one token: no separate x kernel
         torch.cuda.synchronize()
         yn = y.cpu().numpy()
         check_close(yn, ref, TIGHT_L2, TIGHT_MAX, f"call {k}")
