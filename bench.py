@@ -393,7 +393,7 @@ def gpu_decode(cfg, K, warmup, rank, world, dist, path="f32", e2e=False):
     launches = q.q4k_last_call_kernels()
     torch.cuda.synchronize()
     torch.cuda.set_stream(torch.cuda.default_stream())
-    return {"cfg": cfg, "ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms,
+    return {"cfg": cfg, "path": path, "ms": ms, "K": K, "clocks": clocks, "kern_ms": kern_ms, "e2e_ms": e2e_ms,
             "e2e_copy_ms": e2e_copy_ms, "E": E, "R": R, "wbytes": wbytes, "xbytes": x_np.nbytes,
             "launches_per_step": launches, "pct": pct, "G": runs.G, "long_ms": long_ms, "long_K": long_K}
 
@@ -556,6 +556,15 @@ PREFILL_KERNELS = ["q8_1_x", "expand_x", "gate_up_mmq", "expand_h", "down_mmq_an
 DECODE_DTYPE = "f16 hi+lo x (~22-bit), exact f16 q*scale weights, f32 accumulate"
 
 
+def _kernel_slots(r):
+    """The profiling slots (K0, K1, K1b, K2, K3) a decode call used: one token on the float32
+    entry with x in device memory has no K0 (the gate/up GEMV builds x's fragments)."""
+    slots = [0, 1, 2, 3, 4]
+    if r.get("path") == "f32" and r["cfg"].m == 1:
+        slots = slots[1:]
+    return slots[:r["launches_per_step"]]
+
+
 def decode_object(r, pk, pk_kind, names, dtype, kernel_label):
     """The JSON object of one decode leg: rate, per-kernel times and the roofline of the gate/up GEMV."""
     c = r["cfg"]
@@ -566,7 +575,7 @@ def decode_object(r, pk, pk_kind, names, dtype, kernel_label):
     o = {"workload": c.name, "hidden": c.hidden, "inter": c.inter, "m": c.m,
          "value": r["wbytes"] / (step_ms * 1e-3) / 1e9, "unit": "GB/s", "steps": r["K"], "ms_per_step": step_ms,
          "step_frac": (r["wbytes"] / (step_ms * 1e-3) / 1e9) / pk["hbm_gbs"], "dtype": dtype,
-         "kernels_ms": dict(zip(names, r["kern_ms"][:r["launches_per_step"]])),
+         "kernels_ms": {names[i]: r["kern_ms"][i] for i in _kernel_slots(r)},
          "roofline": {"kernel": kernel_label, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"],
                       "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "peak_kind": f"{pk_kind} copy bandwidth",
                       "algorithmic_bytes_per_launch": k1_bytes, "avg_launch_ms": k1_ms},

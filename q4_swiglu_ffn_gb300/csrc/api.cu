@@ -230,7 +230,7 @@ q4k_status run_graphed(const DecodeGraph& key, cudaStream_t s, Launch launch) {
 
 q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const void* wg, const void* wu,
                       const void* wd, void* y, int ybf16, void* ws, DeviceState* d, cudaStream_t s) {
-  g_kernels += q4k::decode_kernels(p, false, ybf16);  // K0 (not for one token), K1, K1b, K2 (+ K3)
+  g_kernels += q4k::decode_kernels(p, false, ybf16, x);  // K0 (not for one token in device memory), K1, K1b, K2 (+ K3)
   DecodeGraph key;
   key.path = 0;
   key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = static_cast<float*>(y);

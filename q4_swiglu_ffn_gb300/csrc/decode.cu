@@ -262,9 +262,10 @@ __device__ __forceinline__ void round_q8_1(float v[8], int8_t q[8], float& d, fl
   for (int i = 0; i < 8; ++i) v[i] = (float)q[i] * d;
 }
 
-// K0: one CTA per superblock of x, one warp per token slot (not launched for one token:
-// the gate/up GEMV builds its block-diagonal fragments itself, diag_frags_from_x).
-template <typename T, bool Q8>
+// K0: one CTA per superblock of x, one warp per token slot. DIAG: one token, x in host
+// memory (with x in device memory the gate/up GEMV builds the block-diagonal fragments
+// itself, diag_frags_from_x, and K0 is not launched).
+template <typename T, bool Q8, bool DIAG = false>
 __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt, FragPtrs f) {
   pdl_launch_dependents();
   const int t = threadIdx.x >> 5, sb = blockIdx.x, lane = threadIdx.x & 31;
@@ -277,7 +278,10 @@ __global__ void prep_x_kernel(const T* __restrict__ x, int hidden, int m, int nt
       round_q8_1(v, q, d, s);
     }
   }
-  frag_token(v, t >= m, t, nt, sb, f);
+  if constexpr (DIAG)
+    frag_token_diag(v, sb, f);
+  else
+    frag_token(v, t >= m, t, nt, sb, f);
 }
 
 // silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
@@ -358,7 +362,8 @@ struct GemvParams {
   float* out;         // chunk sums: [nks][2][m][rows] (gate/up) or [nks][m][rows] (down)
   uint32_t* err;
   int diag;           // one token with block-diagonal B fragments (frag_token_diag)
-  const void* x;      // one-token gate/up: x itself (the fragments are built in the kernel)
+  const void* x;      // one-token gate/up: x itself, the fragments built in the kernel (or null: read
+                      // the records K0 wrote)
   int xbf16;          // ... as bf16 (else float32)
 };
 
@@ -523,7 +528,7 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   int csb = -1;
   if constexpr (DIAG && GATEUP) {  // x's fragments of the first superblock, while the first weights arrive
     const int sb0 = cw.g * SLICES + slice;
-    if (cw.u < u1 && sb0 < min(P.nsb, (cw.ks + 1) * P.gpc * SLICES)) {
+    if (P.x && cw.u < u1 && sb0 < min(P.nsb, (cw.ks + 1) * P.gpc * SLICES)) {
       uint2 bt[16];
       diag_frags_from_x(P.x, P.xbf16, sb0, bt, xlo, xhi, xsc[0]);
 #pragma unroll
@@ -567,11 +572,19 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
           xlo = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig];
           xhi = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig + 1];
           xsc[0] = reinterpret_cast<const float*>(rec + DREC_SC)[0] * 1048576.f;  // 2^e * 2^20
-        } else {  // x's fragments, built here from x (no separate kernel)
+        } else if (P.x) {  // x's fragments, built here from x (no separate kernel)
           uint2 bt[16];
           diag_frags_from_x(P.x, P.xbf16, sb, bt, xlo, xhi, xsc[0]);
 #pragma unroll
           for (int k = 0; k < 16; ++k) bc[k][0] = bt[k];
+        } else {  // x's record, written by K0
+          const uint8_t* rec = reinterpret_cast<const uint8_t*>(P.in.fx) + (int64_t)sb * DREC;
+          const uint2* fxd = reinterpret_cast<const uint2*>(rec);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) bc[k][0] = act ? fxd[k * 8 + g] : make_uint2(0u, 0u);
+          xlo = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig];
+          xhi = reinterpret_cast<const float*>(rec + DREC_X)[2 * tig + 1];
+          xsc[0] = reinterpret_cast<const float*>(rec + DREC_SC)[0] * 1048576.f;  // 2^e * 2^20
         }
         csb = sb;
       }
@@ -847,9 +860,9 @@ cudaError_t launch_gemv(const CUtensorMap& t0, const CUtensorMap& t1, const Gemv
   const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<CUtensorMap*>(&t0), const_cast<CUtensorMap*>(&t1), const_cast<GemvParams*>(&P)};
-  // the one-token gate/up GEMV is the call's first kernel (it builds x's fragments itself)
+  // the one-token gate/up GEMV that builds x's fragments itself is the call's first kernel
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS / S::TPW * S::SLICES * 32), smem, s,
-                    args, !(GATEUP && DIAG));
+                    args, !(GATEUP && DIAG && P.x));
 }
 
 template <bool GATEUP>
@@ -902,9 +915,18 @@ bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePl
   return true;
 }
 
-int decode_kernels(const DecodePlan& p, bool q8, int ybf16) {
-  const bool diag = p.m == 1 && !q8;  // no K0: K1 builds x's fragments
-  return (diag ? 3 : 4) + (p.nks2 > 1 || ybf16);
+bool device_resident(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+int decode_kernels(const DecodePlan& p, bool q8, int ybf16, const void* x) {
+  const bool no_k0 = p.m == 1 && !q8 && device_resident(x);  // K1 builds x's fragments
+  return (no_k0 ? 3 : 4) + (p.nks2 > 1 || ybf16);
 }
 
 cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const void* wg, const void* wu, const void* wd,
@@ -925,12 +947,19 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
       !weight_map(&md, wd, p.hidden, nsb2, 16 * cb2, sl2))
     return cudaErrorInvalidValue;
 
-  // One token on the float32 path: block-diagonal operands (see frag_token_diag). K1 then
-  // builds x's fragments itself and is the call's first kernel (there is no K0).
+  // One token on the float32 path: block-diagonal operands (see frag_token_diag). With x in
+  // device memory K1 builds x's fragments itself and is the call's first kernel (no K0).
+  // With x in host memory K0 reads it once (every K1 warp reading it across the host link
+  // cost several microseconds) and writes the records K1 reads.
   const bool diag = p.m == 1 && !q8;
+  const bool k0 = !diag || !device_resident(x);
   // K0: not a dependent launch, so it also orders this call after the previous one on the stream
   prof.before(0, s);
-  if (!diag) {
+  if (diag && k0 && bf16)
+    prep_x_kernel<__nv_bfloat16, false, true><<<nsb1, 32, 0, s>>>((const __nv_bfloat16*)x, p.hidden, 1, 1, f1);
+  else if (diag && k0)
+    prep_x_kernel<float, false, true><<<nsb1, 32, 0, s>>>((const float*)x, p.hidden, 1, 1, f1);
+  else if (!diag) {
     const int nw = 128 * p.nt;  // one warp per token slot
     if (bf16 && q8)
       prep_x_kernel<__nv_bfloat16, true><<<nsb1, nw, 0, s>>>((const __nv_bfloat16*)x, p.hidden, p.m, p.nt, f1);
@@ -945,7 +974,7 @@ cudaError_t launch_decode(const DecodePlan& p, const void* x, int bf16, const vo
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err, diag, x, bf16};
+  GemvParams g1{p.inter, nsb1, p.m, p.kc1, p.nks1, f1, p1, err, diag, k0 ? nullptr : x, bf16};
   prof.before(1, s);
   e = launch_gemv_nt<true>(p.nt, mg, mu, g1, p.grid1, s);
   prof.after(1, s);

@@ -38,8 +38,10 @@ struct DecodePlan {
   size_t off_fx1, off_fm1, off_sc1, off_fx2, off_fm2, off_sc2, off_p1, off_p2;
 };
 bool decode_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, DecodePlan* p);
-// Kernels one launch_decode call enqueues (q8: with q8h).
-int decode_kernels(const DecodePlan& p, bool q8, int ybf16);
+// Kernels one launch_decode call enqueues (q8: with q8h; x as passed to launch_decode).
+int decode_kernels(const DecodePlan& p, bool q8, int ybf16, const void* x);
+// x (or any pointer) is in device or managed memory (not page-locked host memory).
+bool device_resident(const void* p);
 // y is float32, or bf16 when ybf16 (rounded once by the final chunk-sum kernel).
 // With q8h, x and h are rounded to Q8_1 before they become the B operand, and the
 // Q8_1 of h (quants [m][inter], then (d, s) [m][inter/32]) is stored at q8h.

@@ -66,7 +66,7 @@ q4k_status noalloc_call(const void* x, int64_t m, int64_t hidden, int64_t inter,
   q4k::DecodePlan p;
   if (!q4k::decode_plan(m, hidden, inter, sms, &p)) return Q4K_ERR_SHAPE;
   if (p.ws_bytes > q4k::NOALLOC_SCRATCH_BYTES) return Q4K_ERR_NOMEM;  // more scratch than the array holds
-  q4k::record_kernels(q4k::decode_kernels(p, false, 0));             // K0 (not for one token), K1, K1b, K2 (+ K3)
+  q4k::record_kernels(q4k::decode_kernels(p, false, 0, x));          // K0 (not for one token in device memory), K1, K1b, K2 (+ K3)
   const cudaError_t e = q4k::launch_decode(p, x, 0, W_gate, W_up, W_down, y, scratch, err,
                                            static_cast<cudaStream_t>(stream), q4k::ProfileEvents{});
   return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
