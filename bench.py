@@ -557,11 +557,12 @@ DECODE_DTYPE = "f16 hi+lo x (~22-bit), exact f16 q*scale weights, f32 accumulate
 
 
 def _kernel_slots(r):
-    """The profiling slots (K0, K1, K1b, K2, K3) a decode call used: one token on the float32
-    entry with x in device memory has no K0 (the gate/up GEMV builds x's fragments)."""
+    """The profiling slots (K0, K1, K1b, K2, K3) a decode call used: with x in device memory one
+    token on the float32 entry, and one or two on the Q8_1 entry, have no K0 (the gate/up GEMV
+    takes x itself)."""
     slots = [0, 1, 2, 3, 4]
-    if r.get("path") == "f32" and r["cfg"].m == 1:
-        slots = slots[1:]
+    if (r.get("path") == "f32" and r["cfg"].m == 1) or (r.get("path") == "q8_1" and r["cfg"].m <= 2):
+        slots = slots[1:]  # no K0: the gate/up GEMV takes x itself
     return slots[:r["launches_per_step"]]
 
 

@@ -242,7 +242,7 @@ q4k_status run_decode(const q4k::DecodePlan& p, const void* x, int dtype, const 
 
 q4k_status run_decode_q8(const q4k::DecodeQ8Plan& p, const void* x, int dtype, const void* wg, const void* wu,
                          const void* wd, float* y, void* ws, DeviceState* d, cudaStream_t s) {
-  g_kernels += 4 + (p.nks2 > 1);  // K0, K1, K1b, K2 (+ K3)
+  g_kernels += q4k::decode_q8_kernels(p, x);  // K0 (not for 1-2 tokens in device memory), K1, K1b, K2 (+ K3)
   DecodeGraph key;
   key.path = 1;
   key.x = x, key.wg = wg, key.wu = wu, key.wd = wd, key.ws = ws, key.y = y;

@@ -62,7 +62,52 @@ struct GemvQ8Params {
   const float4* xds;   // {d8, s8} of blocks 2i and 2i+1 of the input: [m][nsb * 4]
   float* out;          // chunk sums: [nks][2][m][rows] (gate/up) or [nks][m][rows] (down)
   uint32_t* err;
+  const void* x;       // gate/up: x itself, quantized in the kernel (or null: xq, xds from K0)
+  int xbf16;           // ... as bf16 (else float32)
 };
+
+// One warp: Q8_1 of token tt's superblock sb of x, as lane (g, tig) of the GEMV reads it from
+// K0's planar output: the 64 quants of blocks 2 tig and 2 tig + 1 (w) and their {d8, s8}
+// (d). Lane L quantizes x[8L .. 8L+7] (q8_1_block8, the stand-alone quantizer's rule, so the
+// bytes are K0's); the lanes of quant group tig then gather lanes 8 tig .. 8 tig + 7.
+__device__ __forceinline__ void q8_frags_from_x(const void* x, int xbf16, int64_t kq, int tt, int sb, uint4 w[4],
+                                                float4& d) {
+  const int lane = threadIdx.x & 31, tig = lane & 3;
+  const int64_t off = (int64_t)tt * kq + (int64_t)sb * QK + lane * 8;
+  float v[8];
+  if (xbf16) {
+    const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(x) + off);
+    const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(u[i] << 16);
+      v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+  int8_t q[8];
+  float dd, ss;
+  q8_1_block8(v, q, dd, ss);
+  const uint32_t w0 = (uint32_t)(uint8_t)q[0] | (uint32_t)(uint8_t)q[1] << 8 | (uint32_t)(uint8_t)q[2] << 16 |
+                      (uint32_t)(uint8_t)q[3] << 24;
+  const uint32_t w1 = (uint32_t)(uint8_t)q[4] | (uint32_t)(uint8_t)q[5] << 8 | (uint32_t)(uint8_t)q[6] << 16 |
+                      (uint32_t)(uint8_t)q[7] << 24;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int la = 8 * tig + 2 * i;
+    w[i].x = __shfl_sync(0xffffffffu, w0, la);
+    w[i].y = __shfl_sync(0xffffffffu, w1, la);
+    w[i].z = __shfl_sync(0xffffffffu, w0, la + 1);
+    w[i].w = __shfl_sync(0xffffffffu, w1, la + 1);
+  }
+  d.x = __shfl_sync(0xffffffffu, dd, 8 * tig);
+  d.y = __shfl_sync(0xffffffffu, ss, 8 * tig);
+  d.z = __shfl_sync(0xffffffffu, dd, 8 * tig + 4);
+  d.w = __shfl_sync(0xffffffffu, ss, 8 * tig + 4);
+}
 
 // dp4a with an unsigned first and a signed second operand.
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -205,11 +250,23 @@ __global__ void __launch_bounds__(COMBOS / TPW * SLICES * 32, CPS)
   int csb = -1;
   auto load_x = [&](int tok, int sb, uint4 w[4], float4& d) {
     const int tt = min(tok, P.m - 1);  // padding tokens read a real token; their sums are never stored
+    if (GATEUP && P.x) {  // warp-uniform: quantize x here (no K0)
+      q8_frags_from_x(P.x, P.xbf16, kq, tt, sb, w, d);
+      return;
+    }
     const uint4* xp = reinterpret_cast<const uint4*>(P.xq + (int64_t)tt * kq + (int64_t)sb * QK + 64 * tig);
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = xp[i];
     d = P.xds[((int64_t)tt * P.nsb + sb) * 4 + tig];
   };
+  if (GATEUP && P.x) {  // the first superblock's activations, while the first weights arrive
+    const int sb0 = cw.g * SLICES + slice;
+    if (cw.u < u1 && sb0 < min(P.nsb, (cw.ks + 1) * P.gpc * SLICES)) {
+#pragma unroll
+      for (int k = 0; k < MT; ++k) load_x(k, sb0, xa[k], xd[k]);
+      csb = sb0;
+    }
+  }
 
 #pragma unroll 1
   while (cw.u < u1) {
@@ -380,8 +437,9 @@ cudaError_t launch_gemv_q8(const CUtensorMap& t0, const CUtensorMap& t1, const G
   const cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem, &attr_set);
   if (e != cudaSuccess) return e;
   void* args[] = {const_cast<CUtensorMap*>(&t0), const_cast<CUtensorMap*>(&t1), const_cast<GemvQ8Params*>(&P)};
+  // the gate/up GEMV that quantizes x itself is the call's first kernel
   return launch_pdl(reinterpret_cast<const void*>(kern), dim3(grid), dim3(S::COMBOS / S::TPW * S::SLICES * 32), smem,
-                    s, args);
+                    s, args, !(GATEUP && P.x));
 }
 
 template <bool GATEUP>
@@ -510,6 +568,11 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
   return true;
 }
 
+int decode_q8_kernels(const DecodeQ8Plan& p, const void* x) {
+  if (p.fpath) return decode_kernels(p.fp, true, 0, x);
+  return (device_resident(x) ? 3 : 4) + (p.nks2 > 1);  // K0 only for x in host memory
+}
+
 cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, const void* wg, const void* wu,
                              const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
                              const ProfileEvents& prof, int ybf16) {
@@ -531,13 +594,15 @@ cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, con
       !weight_map(&md, wd, p.hidden, nsb2, 16 * cb2, sl2))
     return cudaErrorInvalidValue;
 
-  // K0: not a dependent launch, so it also orders this call after the previous one on the stream
+  // K0: not a dependent launch, so it also orders this call after the previous one on the stream.
+  // With x in device memory K1 quantizes it itself and is the call's first kernel instead.
+  const bool k0 = !device_resident(x);
   prof.before(0, s);
-  cudaError_t e = launch_q8_1(x, bf16, p.m, p.hidden, xq, s);
+  cudaError_t e = k0 ? launch_q8_1(x, bf16, p.m, p.hidden, xq, s) : cudaSuccess;
   prof.after(0, s);
   if (e != cudaSuccess) return e;
 
-  GemvQ8Params g1{p.inter, nsb1, p.m, p.kc1, p.nks1, xq, xds, p1, err};
+  GemvQ8Params g1{p.inter, nsb1, p.m, p.kc1, p.nks1, xq, xds, p1, err, k0 ? nullptr : x, bf16};
   prof.before(1, s);
   e = launch_gemv_q8_mt<true>(p.mt, mg, mu, g1, p.grid1, s);
   prof.after(1, s);
@@ -556,7 +621,7 @@ cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, con
     if (e != cudaSuccess) return e;
   }
 
-  GemvQ8Params g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, hq, (const float4*)hds, p2, err};
+  GemvQ8Params g2{p.hidden, nsb2, p.m, p.kc2, p.nks2, hq, (const float4*)hds, p2, err, nullptr, 0};
   prof.before(3, s);
   e = launch_gemv_q8_mt<false>(p.mt, md, md, g2, p.grid2, s);
   prof.after(3, s);

@@ -67,6 +67,8 @@ bool decode_q8_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Decod
 cudaError_t launch_decode_q8(const DecodeQ8Plan& p, const void* x, int bf16, const void* wg, const void* wu,
                              const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
                              const ProfileEvents& prof, int ybf16 = 0);
+// Kernels one launch_decode_q8 call enqueues (x as passed to it).
+int decode_q8_kernels(const DecodeQ8Plan& p, const void* x);
 
 // ---------------------------------------------------------------- Q6_K GEMV (m <= 8)
 struct Q6Plan {
