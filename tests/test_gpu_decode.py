@@ -120,11 +120,13 @@ def test_decode_many_k_chunks(H, I, m):
     check_close(y, ref, TIGHT_L2, TIGHT_MAX, f"h {H} i {I} m {m}")
 
 
-def test_decode_bf16_input_through_ex():
-    c = workloads.small_config(768, 1024, 4, "bf16", ("channels", 0.01, 100.0))
+@pytest.mark.parametrize("m", [1, 4])
+def test_decode_bf16_input_through_ex(m):
+    """bf16 activations: one token (x's fragments built inside the gate/up GEMV) and four."""
+    c = workloads.small_config(768, 1024, m, "bf16", ("channels", 0.01, 100.0))
     wg, wu, wd = workloads.weights(c)
     xf, xb = workloads.activations(c)
-    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(4, 768, 1024), dtype=torch.uint8, device=dev())
+    ws = torch.zeros(lib().ffn_q4k_workspace_bytes(m, 768, 1024), dtype=torch.uint8, device=dev())
     y = lib().ffn_q4k_swiglu_ex(to_dev(xb), to_dev(wg), to_dev(wu), to_dev(wd), ws)
     ref, _ = oracle.ffn_decode(xf, wg, wu, wd)
     check_close(y.cpu().numpy(), ref, TIGHT_L2, TIGHT_MAX)

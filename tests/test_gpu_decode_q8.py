@@ -76,8 +76,11 @@ def test_decode_q8_shape_sweep(H, I, m):
     _check(*_run(c))
 
 
-def test_decode_q8_bf16_input():
-    c = workloads.small_config(1024, 1536, 3, "bf16", ("entries", 0.001, 900.0))
+@pytest.mark.parametrize("m", [1, 2, 3])
+def test_decode_q8_bf16_input(m):
+    """bf16 activations: 1-2 tokens (x quantized inside the gate/up GEMV) and 3 (the float32
+    path's kernels)."""
+    c = workloads.small_config(1024, 1536, m, "bf16", ("entries", 0.001, 900.0))
     _check(*_run(c, bf16=True))
 
 
