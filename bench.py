@@ -468,7 +468,7 @@ def gpu_prefill(cfg, steps, world):
     sampler.stop()
     clocks = sampler.summary(t0, t1)
     ms = e0.elapsed_time(e1) / steps
-    kern_ms = _kernel_ms(q, step, 30, 5)
+    kern_ms = _kernel_ms(q, step, 30, len(PREFILL_KERNELS))
     step()
     launches = q.q4k_last_call_kernels()
     assert q.q4k_check_device_error() == 0
@@ -552,7 +552,7 @@ def whole_job(ms_local: float, units_local: float, dist=None):
 
 DECODE_KERNELS = ["prep_x", "gate_up", "swiglu_frag_h", "down", "down_chunk_sum"]
 Q8_KERNELS = ["q8_1_x", "gate_up", "swiglu_q8_1_h", "down", "down_chunk_sum"]
-PREFILL_KERNELS = ["q8_1_x", "expand_x", "gate_up_mmq", "expand_h", "down_mmq_and_sums"]
+PREFILL_KERNELS = ["quant_expand_x", "gate_up_mmq", "expand_h", "down_mmq_and_sums"]
 DECODE_DTYPE = "f16 hi+lo x (~22-bit), exact f16 q*scale weights, f32 accumulate"
 
 
@@ -592,7 +592,7 @@ def decode_object(r, pk, pk_kind, names, dtype, kernel_label):
 def prefill_object(pre, pk, pk_kind, int8):
     c = pre["cfg"]
     gu_ops = 2 * c.m * c.hidden * c.inter * 2
-    gu_ms = pre["kern_ms"][2]
+    gu_ms = pre["kern_ms"][PREFILL_KERNELS.index("gate_up_mmq")]
     ach = gu_ops / (gu_ms * 1e-3) / 1e12
     burst, sus = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
     o = {"workload": c.name, "hidden": c.hidden, "inter": c.inter, "m": c.m,
@@ -755,7 +755,8 @@ def main():
         gp = pre.get("prefill_27b_h5120_i17408_m2048")
         if gp is not None:
             gu_ops = 2 * c.m * c.hidden * c.inter * 2
-            o["fp16_mmq_gate_up_tops_same_run"] = gu_ops / (gp["kern_ms"][2] * 1e-3) / 1e12
+            gu_ms = gp["kern_ms"][PREFILL_KERNELS.index("gate_up_mmq")]
+            o["fp16_mmq_gate_up_tops_same_run"] = gu_ops / (gu_ms * 1e-3) / 1e12
         line["prefill_fp8_gemm_prototype"] = o
     print(json.dumps(line))
     if dist:

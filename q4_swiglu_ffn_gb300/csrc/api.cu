@@ -283,8 +283,8 @@ q4k_status run_ffn(const void* x, int dtype, int64_t m, int64_t hidden, int64_t 
   } else {
     q4k::PrefillPlan p;
     if (!q4k::prefill_plan(m, hidden, inter, d->sms, &p)) return Q4K_ERR_SHAPE;
-    // Q8_1, expand, MMQ, expand, MMQ (+ the split tail tiles' sum) (+ slice sum / bf16 store)
-    g_kernels = 5 + (p.tail_q > 1) + (p.ksplit > 1 || ybf16);
+    // x quantize+expand, MMQ, expand, MMQ (+ the split tail tiles' sum) (+ slice sum / bf16 store)
+    g_kernels = q4k::prefill_kernels(p, ybf16);
     e = q4k::launch_prefill(p, x, dtype == Q4K_BF16, wg, wu, wd, y, ws, d->err, s, g_prof, ybf16);
   }
   return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;

@@ -181,21 +181,6 @@ __device__ __forceinline__ void frag_token_diag(const float v_in[8], int sb, Fra
   if (lane == 0) reinterpret_cast<float*>(rec + DREC_SC)[0] = __uint_as_float((uint32_t)(127 + e) << 23);
 }
 
-// Loads the 8 inputs of this lane (float32 or bf16, widened exactly).
-__device__ __forceinline__ void load8(const float* p, float v[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float v[8]) {
-  const uint4 a = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
 // One warp, one token: the block-diagonal B operand of superblock sb of x, straight into this
 // lane's registers (the record frag_token_diag would write, as the gate/up GEMV reads it):
 // bc[k] for MMA k, and the sub-block sums and scale of this lane's quant group. Lane L

@@ -98,6 +98,8 @@ struct PrefillPlan {
   size_t off_ypart;       // their partial outputs [ksplit][m][hidden] (ksplit > 1)
 };
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);
+// Kernels one prefill call launches.
+int prefill_kernels(const PrefillPlan& p, int ybf16);
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
                            const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
                            const ProfileEvents& prof, int ybf16 = 0);

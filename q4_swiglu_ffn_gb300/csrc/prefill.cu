@@ -43,6 +43,7 @@
 #include "common.cuh"
 #include "gemv_stream.cuh"
 #include "kernels.h"
+#include "q8_1.cuh"
 #include "tc05.cuh"
 #include "tmap.h"
 
@@ -57,35 +58,31 @@ namespace {
 //   scale[t] = 2^e_t.
 // e_t = exponent(127 * max_j d8_j) - 14.
 
-__global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ qs, const float2* __restrict__ ds,
-                                                     int k, __half* __restrict__ hi, __half* __restrict__ lo,
-                                                     __half* __restrict__ mn, float* __restrict__ scale) {
-  const int t = blockIdx.x, tid = threadIdx.x;
-  const int nblk = k / Q8B;
-  const float2* dsr = ds + (int64_t)t * nblk;
-  float mx = 0.f;
-  for (int j = tid; j < nblk; j += 256) mx = fmaxf(mx, fabsf(dsr[j].x));
-  mx = warp_max(mx);
+// The row exponent e_t from each thread's running maximum of d8 (all 256 threads call it).
+__device__ __forceinline__ int row_exponent(float mx) {
   __shared__ float red[8];
+  const int tid = threadIdx.x;
+  mx = warp_max(mx);
   if ((tid & 31) == 0) red[tid >> 5] = mx;
   __syncthreads();
   mx = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
-  int e = 0;
   const float top = mx * 127.f;
-  if (top > 0.f) e = max((int)((__float_as_uint(top) >> 23) & 0xFF) - 127 - 14, -100);
+  return top > 0.f ? max((int)((__float_as_uint(top) >> 23) & 0xFF) - 127 - 14, -100) : 0;
+}
+
+// The planes of one row from its int8 quants qr[k] and block scales d8 (block j at
+// d8[j * dstride]), given e_t.
+__device__ __forceinline__ void expand_row(const int8_t* qr, const float* d8p, int dstride, int k, int e,
+                                           __half* __restrict__ hr, __half* __restrict__ lr,
+                                           __half* __restrict__ mr) {
+  const int tid = threadIdx.x, lane = tid & 31;
   const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-  if (tid == 0) scale[t] = __uint_as_float((uint32_t)(127 + e) << 23);
-  const int8_t* qr = qs + (int64_t)t * k;
-  __half* hr = hi + (int64_t)t * k;
-  __half* lr = lo ? lo + (int64_t)t * k : nullptr;
-  __half* mr = mn + (int64_t)t * (k / QK) * 64;
-  const int lane = tid & 31;
   for (int base = 0; base < k; base += 2048) {
     const int c = base + tid * 8;  // 8 values; one warp covers one superblock
     if (c >= k) break;             // k % 256 == 0, so whole warps leave together
-    const float d8 = dsr[c / Q8B].x;
+    const float d8 = d8p[(c / Q8B) * dstride];
     const float d8s = d8 * s;  // exact power-of-two scaling
     const uint2 raw = *reinterpret_cast<const uint2*>(qr + c);
     int q[8];
@@ -124,6 +121,62 @@ __global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ 
     if (lane < 16) ms[32 + lane] = __float2half_rn(0.f), ms[48 + lane] = __float2half_rn(0.f);
   }
 }
+
+// The planes of a row already quantized to Q8_1 (h, written by the gate/up MMQ's epilogue).
+__global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ qs, const float2* __restrict__ ds,
+                                                     int k, __half* __restrict__ hi, __half* __restrict__ lo,
+                                                     __half* __restrict__ mn, float* __restrict__ scale) {
+  const int t = blockIdx.x;
+  const int nblk = k / Q8B;
+  const float2* dsr = ds + (int64_t)t * nblk;
+  float mx = 0.f;
+  for (int j = threadIdx.x; j < nblk; j += 256) mx = fmaxf(mx, fabsf(dsr[j].x));
+  const int e = row_exponent(mx);
+  if (threadIdx.x == 0) scale[t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  expand_row(qs + (int64_t)t * k, reinterpret_cast<const float*>(dsr), 2, k, e, hi + (int64_t)t * k,
+             lo ? lo + (int64_t)t * k : nullptr, mn + (int64_t)t * (k / QK) * 64);
+}
+
+// x's row quantized to Q8_1 (the stand-alone quantizer's rule, q8_1_block8) and expanded in
+// one pass: the quants and block scales wait in shared memory (k + k/8 bytes) while the
+// CTA finds e_t. The planes are bit-identical to quantizing x and then expanding it.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_expand_kernel(const T* __restrict__ x, int k, __half* __restrict__ hi,
+                                                           __half* __restrict__ lo, __half* __restrict__ mn,
+                                                           float* __restrict__ scale) {
+  extern __shared__ __align__(16) uint8_t qe_smem[];
+  int8_t* sq = reinterpret_cast<int8_t*>(qe_smem);      // k quants
+  float* sd = reinterpret_cast<float*>(qe_smem + k);    // k/32 block scales (k % 256 == 0: aligned)
+  const int t = blockIdx.x, tid = threadIdx.x;
+  const T* xr = x + (int64_t)t * k;
+  float mx = 0.f;
+  for (int base = 0; base < k; base += 2048) {
+    const int c = base + tid * 8;
+    if (c >= k) break;  // whole warps leave together: the quad shuffles see only live lanes
+    float v[8];
+    load8(xr + c, v);
+    int8_t q[8];
+    float d, ss;
+    q8_1_block8(v, q, d, ss);
+    uint2 packed;
+    packed.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) |
+               ((uint32_t)(uint8_t)q[3] << 24);
+    packed.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) |
+               ((uint32_t)(uint8_t)q[7] << 24);
+    *reinterpret_cast<uint2*>(sq + c) = packed;
+    if ((tid & 3) == 0) sd[c / Q8B] = d;
+    mx = fmaxf(mx, d);
+  }
+  const int e = row_exponent(mx);  // its barrier also publishes sq and sd
+  if (tid == 0) scale[t] = __uint_as_float((uint32_t)(127 + e) << 23);
+  expand_row(sq, sd, 1, k, e, hi + (int64_t)t * k, lo ? lo + (int64_t)t * k : nullptr,
+             mn + (int64_t)t * (k / QK) * 64);
+}
+
+// The largest k the fused x kernel takes (its shared memory stays under the 48 KB default);
+// beyond it x is quantized and expanded by two kernels.
+constexpr int QE_MAX_K = 43520;
+inline size_t quant_expand_smem(int64_t k) { return (size_t)k + (size_t)(k / Q8B) * 4; }
 
 // ------------------------------------------------------------------------- tcgen05 MMQ
 constexpr int TM = 128;                   // weight rows per tile
@@ -651,6 +704,10 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   return true;
 }
 
+int prefill_kernels(const PrefillPlan& p, int ybf16) {
+  return (p.hidden <= QE_MAX_K ? 4 : 5) + (p.tail_q > 1) + (p.ksplit > 1 || ybf16);
+}
+
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
                            const void* wd, void* y, void* ws, uint32_t* err, cudaStream_t s,
                            const ProfileEvents& prof, int ybf16) {
@@ -681,14 +738,23 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
       !make_map(&mh_lo, ho.lo, m, I) || !make_map(&mh_mn, ho.mn, m, (I / QK) * 64))
     return cudaErrorInvalidValue;
 
-  prof.before(0, s);
-  cudaError_t e = launch_q8_1(x, bf16, m, H, xq, s);
+  prof.before(0, s);  // x's operand planes
+  cudaError_t e = cudaSuccess;
+  if (H <= QE_MAX_K) {
+    const size_t sm = quant_expand_smem(H);
+    if (bf16)
+      quant_expand_kernel<__nv_bfloat16><<<(unsigned)m, 256, sm, s>>>((const __nv_bfloat16*)x, (int)H, xo.hi,
+                                                                      xo.lo, xo.mn, xo.scale);
+    else
+      quant_expand_kernel<float><<<(unsigned)m, 256, sm, s>>>((const float*)x, (int)H, xo.hi, xo.lo, xo.mn,
+                                                              xo.scale);
+    e = cudaGetLastError();
+  } else if ((e = launch_q8_1(x, bf16, m, H, xq, s)) == cudaSuccess) {
+    expand_kernel<<<(unsigned)m, 256, 0, s>>>(xq, xds, (int)H, xo.hi, xo.lo, xo.mn, xo.scale);
+    e = cudaGetLastError();
+  }
   prof.after(0, s);
   if (e != cudaSuccess) return e;
-  prof.before(1, s);
-  expand_kernel<<<(unsigned)m, 256, 0, s>>>(xq, xds, (int)H, xo.hi, xo.lo, xo.mn, xo.scale);
-  prof.after(1, s);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const int ntn = (int)((m + TN - 1) / TN);
   MmqParams g{};
@@ -705,14 +771,14 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.hq_qs = hq;
   g.hq_ds = hds;
   g.err = err;
-  prof.before(2, s);
+  prof.before(1, s);
   e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s);
-  prof.after(2, s);
+  prof.after(1, s);
   if (e != cudaSuccess) return e;
 
-  prof.before(3, s);
+  prof.before(2, s);
   expand_kernel<<<(unsigned)m, 256, 0, s>>>(hq, hds, (int)I, ho.hi, ho.lo, ho.mn, ho.scale);
-  prof.after(3, s);
+  prof.after(2, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   MmqParams dn{};
@@ -734,7 +800,7 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   const bool fin = p.ksplit > 1 || ybf16;  // the slice sum and/or the bf16 store
   dn.y = fin ? ypart : (float*)y;
   dn.err = err;
-  prof.before(4, s);  // the down MMQ, and the sum of its K slices when there are several
+  prof.before(3, s);  // the down MMQ, and the sum of its K slices when there are several
   e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s)
                    : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s);
   if (e == cudaSuccess && p.tail_q > 1) {
@@ -744,7 +810,7 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
     e = cudaGetLastError();
   }
   if (e == cudaSuccess && fin) e = launch_finish_down(ypart, p.ksplit, m * H, y, ybf16, s);
-  prof.after(4, s);
+  prof.after(3, s);
   return e;
 }
 

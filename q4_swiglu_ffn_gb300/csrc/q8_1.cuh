@@ -11,6 +11,21 @@
 
 namespace q4k {
 
+// Eight consecutive activations (16-byte aligned), float32 or bf16, widened exactly to float32.
+__device__ __forceinline__ void load8(const float* p, float v[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float v[8]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 // The 4 lanes of a block must be aligned quads of the warp, and every lane of
 // the warp must call this (it shuffles).
 __device__ __forceinline__ void q8_1_block8(const float v[8], int8_t q[8], float& d, float& s) {

@@ -60,24 +60,6 @@ cudaError_t launch_dequant(const void* w, float* out, int64_t rows, int64_t cols
 // operations are written with explicit round-to-nearest intrinsics:
 // d = amax/127, inv = 127/amax, q = roundf(x*inv) (ties away from zero), s = d*sum(q).
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float v[8]);
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float v[8]) {
-  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float v[8]) {
-  const uint4 a = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-template <typename T>
 __global__ void q8_1_kernel(const T* __restrict__ x, int8_t* __restrict__ qs, float2* __restrict__ ds,
                             int64_t m, int64_t k) {
   // one thread per 8 values; 4 threads per Q8_1 block; rows of k values
@@ -88,7 +70,7 @@ __global__ void q8_1_kernel(const T* __restrict__ x, int8_t* __restrict__ qs, fl
   const int64_t g = active ? gid : 0;
   const int64_t row = g / per_row, c8 = (g % per_row) * 8;
   float v[8];
-  load8<T>(x + row * k + c8, v);
+  load8(x + row * k + c8, v);
   int8_t q[8];
   float d, s;
   q8_1_block8(v, q, d, s);  // all lanes of the warp take part in the shuffles
@@ -159,7 +141,7 @@ __global__ void quantize_weights_kernel(const T* __restrict__ w, uint8_t* __rest
   const int lane = threadIdx.x & 31, j = lane >> 2;
   const int64_t row = blk / nb_per_row, c = (blk % nb_per_row) * QK + lane * 8;
   float vf[8];
-  load8<T>(w + row * (int64_t)nb_per_row * QK + c, vf);
+  load8(w + row * (int64_t)nb_per_row * QK + c, vf);
   double x[8];
   double mn = 0.0, mx = 0.0;
 #pragma unroll

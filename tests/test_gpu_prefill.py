@@ -99,3 +99,12 @@ def test_prefill_repeatable():
     y1 = lib().ffn_q4k_swiglu_ex(xd, wg, wu, wd, ws).cpu().numpy()
     y2 = lib().ffn_q4k_swiglu_ex(xd, wg, wu, wd, ws).cpu().numpy()
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+@pytest.mark.parametrize("H", [43520, 43776])
+def test_prefill_widest_hidden_sizes(H):
+    """x's row is quantized and expanded by one kernel up to hidden 43520 (its quants and block
+    scales held in shared memory) and by two kernels above that; both sides of the boundary."""
+    c = workloads.small_config(H, 256, 25, "bf16", ("channels", 0.01, 100.0))
+    y, ref, hq, wd = _run(c)
+    _check(y, ref, hq, wd)
