@@ -1,7 +1,7 @@
 // Prefill regime (m >= 25 tokens) of the Q4_K SwiGLU FFN on sm_103a.
 //
-//   P0 q8_1(x)             x -> planar Q8_1 (bit-exact; also the ABI's q8_1_quantize_act)
-//   P1 expand(xq)          Q8_1 -> tensor-core B operand planes (below)
+//   P0 quant_expand(x)     x -> Q8_1 (the ABI's q8_1_quantize_act rule) -> tensor-core B
+//                          operand planes (below), in one pass per token row
 //   P2 mmq<gate/up>        G = deq(Wg) . deq(xq), U = deq(Wu) . deq(xq) on tcgen05,
 //                          h = silu(G) * U, h -> planar Q8_1 (hq)
 //   P3 expand(hq)
@@ -24,10 +24,15 @@
 //                               the 4-bit quants by transform warps and stored
 //                               straight into tensor memory (row i in TMEM lane i),
 //                               so the weights never pass through shared memory.
-//   B (activations, N = 128):   v = q8 * d8 * 2^-e_t split into fp16 hi and lo
+//   B (activations, 128 tokens): v = q8 * d8 * 2^-e_t split into fp16 hi and lo
 //                               (about 22 bits of v; e_t per token keeps |v| < 2^15).
-// Each superblock (256 k) accumulates into its own TMEM buffer; the epilogue
-// warps add d * D_main - 64*dmin * D_min into registers, where D_min is one
+//                               The stage's hi tile and lo tile lie back to back, so
+//                               one N = 256 MMA takes both: D_main columns 0-127 get
+//                               A . hi, 128-255 A . lo. (An MMA costs about the same
+//                               time at N = 128 as at N = 256 on this part, so the
+//                               wide one nearly halves the tensor time.)
+// Each superblock (256 k) accumulates into D_main afresh; the epilogue warps add
+// d * (D_hi + D_lo) - 64*dmin * D_min into registers, where D_min is one
 // K = 16 MMA of the 6-bit mins against s8_j * 2^-(e_t+6) (hi and lo), s8_j =
 // d8_j * sum(q8) of sub-block j. The closed form per output is
 //   sum_b [ d_b * sum_j scale_j * sum_i q_i * v_i  -  dmin_b * sum_j min_j * s8_j ],
@@ -188,8 +193,10 @@ constexpr int TILE_BYTES = TM * KCH * 2;  // 16 KB
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // B hi and lo; A of the stage is in TMEM
 constexpr int NWARPS = 14;                // 0 TMA, 1 MMA, 2-5 transform, 6-13 epilogue
 constexpr int W_TMA = 0, W_MMA = 1, W_EPI = 6, N_EPI = 8;  // warps W_MMA + 1 .. W_EPI - 1 transform
-// TMEM columns: D_main[2] at 0/128 (fp32), D_min at 256, the A tile of stage s at
-// 384 + 32 s (64 fp16 per lane, two to a column)
+// TMEM columns: D_main at 0 (fp32, hi products in 0-127, lo in 128-255), D_min at 256,
+// the A tile of stage s at 384 + 32 s (64 fp16 per lane, two to a column). D_main and
+// D_min have one buffer each: the next superblock's MMAs wait until the epilogue has
+// read them.
 constexpr uint32_t TMEM_COLS = 512, TM_DMIN = 256, TM_A = 384, A_COLS = KCH / 2;
 static_assert(TM_A + STAGES * A_COLS <= TMEM_COLS, "A stages fit in TMEM");
 // gate/up exchange: [128 rows][TN + 1] raw sums, then the TN token factors 2^e_t
@@ -220,7 +227,8 @@ struct MmqParams {
   uint32_t* err;
 };
 
-constexpr uint32_t IDESC = idesc_f16(TM, TN);
+constexpr uint32_t IDESC_MAIN = idesc_f16(TM, 2 * TN);  // B = the hi tile, then the lo tile
+constexpr uint32_t IDESC_MIN = idesc_f16(TM, TN);
 
 // silu(z) = z * sigmoid(z), with t = e^-|z| in (0, 1]: sigmoid is 1 / (1 + t) for z >= 0
 // and t / (1 + t) below. Nothing overflows, the divisor is in [1, 2], where CUDA's
@@ -293,9 +301,9 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
   float* xg = reinterpret_cast<float*>(smem + STAGES * STAGE_BYTES);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + XG_BYTES);
   uint64_t* empty = full + STAGES;
-  uint64_t* accf = empty + STAGES;
-  uint64_t* acce = accf + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* accf = empty + STAGES;  // D_main and D_min hold a finished superblock
+  uint64_t* acce = accf + 1;        // ... and the epilogue has read them
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,10 +344,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       mbar_init(&full[s], 5);   // 4 transform warps + the TMA producer
       mbar_init(&empty[s], 1);  // one tcgen05.commit
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);      // tcgen05.commit
-      mbar_init(&acce[b], N_EPI);  // the epilogue warps
-    }
+    mbar_init(accf, 1);      // tcgen05.commit
+    mbar_init(acce, N_EPI);  // the epilogue warps
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -391,13 +397,13 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       for (int w = blockIdx.x; w < P.nwork && ok; w += gridDim.x) {
         const int nsbl = work(w).nsbl;
         for (int sb = 0; sb < nsbl && ok; ++sb, ++G) {
-          const int ab = G & 1;
-          if (G >= 2 && !wait_bar(&acce[ab], ((G - 2) >> 1) & 1, abort_flag, P.err)) {
+          // one buffer: the epilogue must have read the previous superblock's D_main and D_min
+          if (G >= 1 && !wait_bar(acce, (G - 1) & 1, abort_flag, P.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_main = tmem + ab * TN, d_min = tmem + TM_DMIN;
+          const uint32_t d_main = tmem, d_min = tmem + TM_DMIN;
           for (int c = 0; c < CH_PER_SB; ++c, ++q) {
             const int s = q % STAGES, u = q / STAGES;
             if (!wait_bar(&full[s], u & 1, abort_flag, P.err)) {
@@ -406,27 +412,20 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             }
             tc_fence_after();
             const uint32_t st = smem_u32(smem + s * STAGE_BYTES), a = tmem + TM_A + s * A_COLS;
-            const uint64_t b0 = sw128_desc(st), b1 = sw128_desc(st + TILE_BYTES);
+            const uint64_t b0 = sw128_desc(st);  // hi rows 0-127, then lo rows (the next 16 KB)
             if (c < 4) {
 #pragma unroll
               for (int ks = 0; ks < KCH / 16; ++ks) {
                 const uint64_t off = (uint64_t)((ks * 32) >> 4);  // 16 fp16 = 32 bytes along K
-                mma_f16_ts(d_main, a + ks * 8, b0 + off, IDESC, (c | ks) != 0);  // 16 fp16 = 8 TMEM columns
-                mma_f16_ts(d_main, a + ks * 8, b1 + off, IDESC, 1u);
+                mma_f16_ts(d_main, a + ks * 8, b0 + off, IDESC_MAIN, (c | ks) != 0);  // 16 fp16 = 8 TMEM columns
               }
             } else {
-              // D_min has one buffer: the epilogue must have read the previous superblock's
-              if (G >= 1 && !wait_bar(&acce[(G - 1) & 1], ((G - 1) >> 1) & 1, abort_flag, P.err)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              mma_f16_ts(d_min, a, b0, IDESC, 0u);
+              mma_f16_ts(d_min, a, b0, IDESC_MIN, 0u);
             }
             mma_commit(&empty[s]);
           }
           if (!ok) break;
-          mma_commit(&accf[ab]);
+          mma_commit(accf);
         }
       }
     }
@@ -512,26 +511,28 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 #pragma unroll
       for (int i = 0; i < TN / 2; ++i) acc[i] = 0.f;
       for (int sb = 0; sb < k.nsbl; ++sb, ++G) {
-        const int ab = G & 1;
         if (!ok) continue;
         const uint32_t dm2 = __ldg(reinterpret_cast<const uint32_t*>(hdr + (int64_t)sb * BLK));
         const float d = fp16_bits_to_f32(dm2), dmn = -64.f * fp16_bits_to_f32(dm2 >> 16);
-        ok = __all_sync(0xffffffffu, wait_bar(&accf[ab], (G >> 1) & 1, abort_flag, P.err));
+        ok = __all_sync(0xffffffffu, wait_bar(accf, G & 1, abort_flag, P.err));
         if (!ok) continue;
         tc_fence_after();
-        const uint32_t tm_main = tmem + lane_addr + ab * TN + c0, tm_min = tmem + lane_addr + TM_DMIN + c0;
+        const uint32_t tm_hi = tmem + lane_addr + c0, tm_min = tmem + lane_addr + TM_DMIN + c0;
 #pragma unroll
         for (int j = 0; j < TN / 32; ++j) {
-          float v[16], u[16];
-          tmem_ld16(tm_main + j * 16, v);
+          float v[16], vl[16], u[16];
+          tmem_ld16(tm_hi + j * 16, v);
+          tmem_ld16(tm_hi + TN + j * 16, vl);
           tmem_ld16(tm_min + j * 16, u);
           tmem_wait_ld();
+          if (j == TN / 32 - 1) {  // every column of this warp is in registers: release the buffers
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce);
+          }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(u[i], dmn, fmaf(v[i], d, acc[j * 16 + i]));
+          for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(u[i], dmn, fmaf(v[i] + vl[i], d, acc[j * 16 + i]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[ab]);
       }
       if (!ok) *abort_flag = 1;
       const int t0 = k.nt * TN;
