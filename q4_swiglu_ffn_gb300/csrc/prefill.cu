@@ -227,6 +227,15 @@ struct MmqParams {
   uint32_t* err;
 };
 
+// The transform warps load each superblock of their rows one superblock ahead into
+// registers, and PF_SB superblocks ahead into L2.
+constexpr int PF_SB = 3;
+__device__ __forceinline__ void prefetch_row_l2(const uint8_t* p) {  // the <= 3 lines of a 144-byte block
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p + 128));
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p + BLK - 1));
+}
+
 constexpr uint32_t IDESC_MAIN = idesc_f16(TM, 2 * TN);  // B = the hi tile, then the lo tile
 constexpr uint32_t IDESC_MIN = idesc_f16(TM, TN);
 
@@ -438,9 +447,24 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     if (w < P.nwork) {
       Work k = work(w);
       const uint8_t* src = row_ptr(k, r);
+      // the next item's row (for the prefetches that run past this item's last superblock)
+      auto next_row = [&](int wc, int& nsbl) -> const uint8_t* {
+        if (wc + (int)gridDim.x >= P.nwork) {
+          nsbl = 0;
+          return nullptr;
+        }
+        const Work kn = work(wc + gridDim.x);
+        nsbl = kn.nsbl;
+        return row_ptr(kn, r);
+      };
+      int nsbl_n;
+      const uint8_t* src_n = next_row(w, nsbl_n);
       uint4 raw[9];
 #pragma unroll
       for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+#pragma unroll
+      for (int a = 1; a < PF_SB; ++a)
+        if (a < k.nsbl) prefetch_row_l2(src + (int64_t)a * BLK);
       int q = 0;
       bool ok = true;
       while (ok) {
@@ -458,6 +482,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 #pragma unroll
             for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(nxt) + i);
           }
+          // and the superblock PF_SB ahead into L2, so that the load above finds it there
+          const int ahead = sb + PF_SB;
+          if (ahead < k.nsbl)
+            prefetch_row_l2(src + (int64_t)ahead * BLK);
+          else if (ahead - k.nsbl < nsbl_n)
+            prefetch_row_l2(src_n + (int64_t)(ahead - k.nsbl) * BLK);
           const uint4 hd = cur[0];
           uint32_t scs[8], mns[8];  // all 6-bit scales and mins of this superblock
 #pragma unroll
@@ -491,6 +521,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         if (w >= P.nwork) break;
         k = work(w);
         src = row_ptr(k, r);
+        src_n = next_row(w, nsbl_n);
       }
     }
   } else {
