@@ -248,29 +248,39 @@ __device__ __forceinline__ float silu_f(float z) {
   return z * __fdividef(z >= 0.f ? 1.0f : t, 1.0f + t);
 }
 
-// SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7).
-// xg holds, per tile row (0-63 gate, 64-127 up, same 64 inter indices), the
-// 128 token columns; ts (after xg) their factors 2^e_t. Each of the 256 threads
-// owns one item (token e % 128, Q8_1 block e / 128 of 32 inter rows) whole: its
-// 32 values are independent, so the max and the sum need no shuffles, and its 32
-// quants leave as two 16-byte stores. Reading column tt of a row, the lanes of a
-// warp hit consecutive banks (the row pitch is 129 words).
-__device__ __forceinline__ void gateup_final(const float* xg, const MmqParams& P, int mt, int nt, int ew,
-                                             int lane, volatile int* abort_flag) {
+// SwiGLU + Q8_1 of a finished gate/up tile, shared by 8 warps (ew = 0..7), in
+// FINAL_PIECES steps so that the epilogue can run them between the next item's
+// superblock hand-overs instead of holding the MMAs up. xg holds, per tile row (0-63
+// gate, 64-127 up, same 64 inter indices), the 128 token columns; ts (after xg) their
+// factors 2^e_t. Each of the 256 threads owns one item (token e % 128, Q8_1 block
+// e / 128 of 32 inter rows) whole: its 32 values are independent, so the max and the
+// sum need no shuffles, and its 32 quants leave as two 16-byte stores. Steps 0-3 each
+// turn 8 of the item's gate values into h = silu(g) * u in place (the item owns those
+// rows of its column) and carry the running max; step 4 quantizes and stores. Reading
+// column tt of a row, the lanes of a warp hit consecutive banks (the row pitch is 129
+// words).
+constexpr int FINAL_PIECES = 5;
+__device__ __forceinline__ void gateup_final_piece(float* xg, const MmqParams& P, int mt, int nt, int ew, int lane,
+                                                   int piece, float& amax, volatile int* abort_flag) {
   if (*abort_flag) return;
   constexpr int LD = TN + 1;
   const float* ts = xg + TM * LD;
   const int e = ew * 32 + lane, tt = e & (TN - 1), qb = e / TN;
   const int t = nt * TN + tt;
   if (t >= P.m) return;
-  const float sc = ts[tt];
-  float h[Q8B], amax = 0.f;
+  float* col = xg + (qb * 32) * LD + tt;  // row qb*32 + j of this item at col[j * LD]
+  if (piece < 4) {
+    const float sc = ts[tt];
 #pragma unroll
-  for (int j = 0; j < Q8B; ++j) {
-    const float g = xg[(qb * 32 + j) * LD + tt] * sc;
-    const float u = xg[(64 + qb * 32 + j) * LD + tt] * sc;
-    h[j] = silu_f(g) * u;
-    amax = fmaxf(amax, fabsf(h[j]));
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = piece * 8 + jj;
+      const float g = col[j * LD] * sc;
+      const float u = col[(64 + j) * LD] * sc;
+      const float h = silu_f(g) * u;
+      col[j * LD] = h;
+      amax = fmaxf(amax, fabsf(h));
+    }
+    return;
   }
   const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
   const float dq = nz ? __fdiv_rn(amax, 127.f) : 0.f;
@@ -282,7 +292,7 @@ __device__ __forceinline__ void gateup_final(const float* xg, const MmqParams& P
     uint32_t v = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      float rq = roundf(__fmul_rn(h[4 * w + b], inv));
+      float rq = roundf(__fmul_rn(col[(4 * w + b) * LD], inv));
       rq = fminf(fmaxf(rq, -127.f), 127.f);
       const int qi = (int)rq;
       sum += qi;
@@ -535,6 +545,13 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     constexpr int LD = TN + 1;
     int G = 0;  // superblocks consumed so far (all items)
     bool ok = true;
+    // gate/up: the previous item's SwiGLU + Q8_1 steps still to run (FINAL_PIECES when none)
+    int pend_mt = 0, pend_nt = 0, pend_piece = FINAL_PIECES;
+    float pend_amax = 0.f;
+    auto final_step = [&]() {
+      gateup_final_piece(xg, P, pend_mt, pend_nt, warp - W_EPI, lane, pend_piece, pend_amax, abort_flag);
+      ++pend_piece;
+    };
     for (int w = blockIdx.x; w < P.nwork; w += gridDim.x) {
       const Work k = work(w);
       const uint8_t* hdr = row_ptr(k, r);
@@ -564,12 +581,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(u[i], dmn, fmaf(v[i] + vl[i], d, acc[j * 16 + i]));
         }
+        // one step of the previous item's tail while the MMAs run this item's next superblock
+        if (GATEUP && pend_piece < FINAL_PIECES) final_step();
       }
       if (!ok) *abort_flag = 1;
       const int t0 = k.nt * TN;
       if (GATEUP) {
-        // rows 0-63 hold gate, 64-127 up, for the same 64 inter indices; the previous
-        // item's SwiGLU pass has finished reading the exchange before it is rewritten
+        // rows 0-63 hold gate, 64-127 up, for the same 64 inter indices. The previous
+        // item's tail (steps left over when this item had fewer superblocks than steps)
+        // finishes, and every warp is past it, before the exchange is rewritten.
+        while (pend_piece < FINAL_PIECES) final_step();
         __syncwarp();
         asm volatile("bar.sync 2, 256;" ::: "memory");
 #pragma unroll
@@ -577,7 +598,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         if (half == 0) xg[TM * LD + r] = t0 + r < P.m ? P.tscale[t0 + r] : 0.f;  // thread r: token r's factor
         __syncwarp();
         asm volatile("bar.sync 2, 256;" ::: "memory");
-        gateup_final(xg, P, k.mt, k.nt, warp - W_EPI, lane, abort_flag);
+        pend_mt = k.mt, pend_nt = k.nt, pend_piece = 0, pend_amax = 0.f;
       } else if (ok && k.tl >= 0) {
         // a slice of a split tail tile: its partial tile, token-major, rows contiguous
         float* so = P.tail + ((int64_t)k.ks * (P.tiles - P.whole) + k.tl) * TM * TN;
@@ -596,6 +617,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         }
       }
     }
+    if (GATEUP)
+      while (pend_piece < FINAL_PIECES) final_step();  // the last item's tail
   }
   // ---------------------------------------------------------------- teardown
   // (lane 0 of the TMA and MMA warps arrives after its loop, the other lanes long before)
