@@ -58,22 +58,24 @@ namespace q4k {
 namespace {
 
 // ------------------------------------------------------------------------- expand
-// One CTA (256 threads) per token row. Writes
+// One CTA (EXP_NT threads) per token row. Writes
 //   hi[t][k], lo[t][k]  fp16 planes of q8*d8*2^-e_t at permuted positions,
 //   mn[t][sb*64 + 0..15] fp16 of s8_j*2^-(e_t+6): hi of the 8 sub-blocks, then lo,
 //   scale[t] = 2^e_t.
 // e_t = exponent(127 * max_j d8_j) - 14.
 
-// The row exponent e_t from each thread's running maximum of d8 (all 256 threads call it).
+constexpr int EXP_NT = 256;  // threads of an expand CTA
+
+// The row exponent e_t from each thread's running maximum of d8 (all EXP_NT threads call it).
 __device__ __forceinline__ int row_exponent(float mx) {
-  __shared__ float red[8];
+  __shared__ float red[EXP_NT / 32];
   const int tid = threadIdx.x;
   mx = warp_max(mx);
   if ((tid & 31) == 0) red[tid >> 5] = mx;
   __syncthreads();
   mx = red[0];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
+  for (int i = 1; i < EXP_NT / 32; ++i) mx = fmaxf(mx, red[i]);
   const float top = mx * 127.f;
   return top > 0.f ? max((int)((__float_as_uint(top) >> 23) & 0xFF) - 127 - 14, -100) : 0;
 }
@@ -85,7 +87,7 @@ __device__ __forceinline__ void expand_row(const int8_t* qr, const float* d8p, i
                                            __half* __restrict__ mr) {
   const int tid = threadIdx.x, lane = tid & 31;
   const float s = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e
-  for (int base = 0; base < k; base += 2048) {
+  for (int base = 0; base < k; base += EXP_NT * 8) {
     const int c = base + tid * 8;  // 8 values; one warp covers one superblock
     if (c >= k) break;             // k % 256 == 0, so whole warps leave together
     const float d8 = d8p[(c / Q8B) * dstride];
@@ -129,14 +131,14 @@ __device__ __forceinline__ void expand_row(const int8_t* qr, const float* d8p, i
 }
 
 // The planes of a row already quantized to Q8_1 (h, written by the gate/up MMQ's epilogue).
-__global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ qs, const float2* __restrict__ ds,
+__global__ void __launch_bounds__(EXP_NT) expand_kernel(const int8_t* __restrict__ qs, const float2* __restrict__ ds,
                                                      int k, __half* __restrict__ hi, __half* __restrict__ lo,
                                                      __half* __restrict__ mn, float* __restrict__ scale) {
   const int t = blockIdx.x;
   const int nblk = k / Q8B;
   const float2* dsr = ds + (int64_t)t * nblk;
   float mx = 0.f;
-  for (int j = threadIdx.x; j < nblk; j += 256) mx = fmaxf(mx, fabsf(dsr[j].x));
+  for (int j = threadIdx.x; j < nblk; j += EXP_NT) mx = fmaxf(mx, fabsf(dsr[j].x));
   const int e = row_exponent(mx);
   if (threadIdx.x == 0) scale[t] = __uint_as_float((uint32_t)(127 + e) << 23);
   expand_row(qs + (int64_t)t * k, reinterpret_cast<const float*>(dsr), 2, k, e, hi + (int64_t)t * k,
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(256) expand_kernel(const int8_t* __restrict__ 
 // one pass: the quants and block scales wait in shared memory (k + k/8 bytes) while the
 // CTA finds e_t. The planes are bit-identical to quantizing x and then expanding it.
 template <typename T>
-__global__ void __launch_bounds__(256) quant_expand_kernel(const T* __restrict__ x, int k, __half* __restrict__ hi,
+__global__ void __launch_bounds__(EXP_NT) quant_expand_kernel(const T* __restrict__ x, int k, __half* __restrict__ hi,
                                                            __half* __restrict__ lo, __half* __restrict__ mn,
                                                            float* __restrict__ scale) {
   extern __shared__ __align__(16) uint8_t qe_smem[];
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(256) quant_expand_kernel(const T* __restrict__
   const int t = blockIdx.x, tid = threadIdx.x;
   const T* xr = x + (int64_t)t * k;
   float mx = 0.f;
-  for (int base = 0; base < k; base += 2048) {
+  for (int base = 0; base < k; base += EXP_NT * 8) {
     const int c = base + tid * 8;
     if (c >= k) break;  // whole warps leave together: the quad shuffles see only live lanes
     float v[8];
@@ -799,14 +801,14 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   if (H <= QE_MAX_K) {
     const size_t sm = quant_expand_smem(H);
     if (bf16)
-      quant_expand_kernel<__nv_bfloat16><<<(unsigned)m, 256, sm, s>>>((const __nv_bfloat16*)x, (int)H, xo.hi,
+      quant_expand_kernel<__nv_bfloat16><<<(unsigned)m, EXP_NT, sm, s>>>((const __nv_bfloat16*)x, (int)H, xo.hi,
                                                                       xo.lo, xo.mn, xo.scale);
     else
-      quant_expand_kernel<float><<<(unsigned)m, 256, sm, s>>>((const float*)x, (int)H, xo.hi, xo.lo, xo.mn,
+      quant_expand_kernel<float><<<(unsigned)m, EXP_NT, sm, s>>>((const float*)x, (int)H, xo.hi, xo.lo, xo.mn,
                                                               xo.scale);
     e = cudaGetLastError();
   } else if ((e = launch_q8_1(x, bf16, m, H, xq, s)) == cudaSuccess) {
-    expand_kernel<<<(unsigned)m, 256, 0, s>>>(xq, xds, (int)H, xo.hi, xo.lo, xo.mn, xo.scale);
+    expand_kernel<<<(unsigned)m, EXP_NT, 0, s>>>(xq, xds, (int)H, xo.hi, xo.lo, xo.mn, xo.scale);
     e = cudaGetLastError();
   }
   prof.after(0, s);
@@ -833,7 +835,7 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   if (e != cudaSuccess) return e;
 
   prof.before(2, s);
-  expand_kernel<<<(unsigned)m, 256, 0, s>>>(hq, hds, (int)I, ho.hi, ho.lo, ho.mn, ho.scale);
+  expand_kernel<<<(unsigned)m, EXP_NT, 0, s>>>(hq, hds, (int)I, ho.hi, ho.lo, ho.mn, ho.scale);
   prof.after(2, s);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
