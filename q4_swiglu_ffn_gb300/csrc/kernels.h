@@ -95,6 +95,8 @@ struct PrefillPlan {
   int num_sms;            // SMs (resident CTAs of the GEMMs, for their tile order)
   int tail_whole, tail_q; // down projection: tiles from tail_whole on split into tail_q K slices
   size_t off_tail;        // their partial tiles
+  int gu_whole, gu_q;     // the same for the gate/up projection (its SwiGLU after the slices' sum)
+  size_t off_gtail;       // their partial tiles
   size_t off_ypart;       // their partial outputs [ksplit][m][hidden] (ksplit > 1)
 };
 bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, PrefillPlan* p);

@@ -216,10 +216,12 @@ struct MmqParams {
   int ksplit;          // slices of K (down only; 1 for gate/up)
   int tiles;           // (row tile, token tile) pairs
   int nwork;           // work items: tiles x ksplit; item w is slice w / tiles of tile w % tiles
-  // Down only, without SPLIT: the tiles from `whole` on (the last, partial round of
-  // items on the SMs) are split along K into tail_q > 1 slices, items whole + j for
+  // Without SPLIT: the tiles from `whole` on (the last, partial round of items on the
+  // SMs) are split along K into tail_q > 1 slices, items whole + j for
   // j < (tiles - whole) * tail_q (slice j / (tiles - whole) of tile whole + j % (tiles -
   // whole)), which store partial tiles [tail_q][tiles - whole][TN tokens][TM rows] in tail
+  // (scaled by the token factors 2^e_t; for gate/up the raw g and u, SwiGLU and Q8_1 come
+  // after the slices' sum)
   int whole, tail_q;
   float* tail;
   int mt_fast;         // consecutive CTAs take consecutive row tiles (else consecutive token tiles)
@@ -340,7 +342,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     k.tl = -1;
     k.ks = SPLIT ? w / P.tiles : 0;
     int tile = w - k.ks * P.tiles;
-    if (!SPLIT && !GATEUP && P.tail_q > 1 && w >= P.whole) {
+    if (!SPLIT && P.tail_q > 1 && w >= P.whole) {
       const int j = w - P.whole, ntail = P.tiles - P.whole;
       k.tl = j % ntail;
       k.ks = j / ntail;
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       }
       if (!ok) *abort_flag = 1;
       const int t0 = k.nt * TN;
-      if (GATEUP) {
+      if (GATEUP && k.tl < 0) {
         // rows 0-63 hold gate, 64-127 up, for the same 64 inter indices. The previous
         // item's tail (steps left over when this item had fewer superblocks than steps)
         // finishes, and every warp is past it, before the exchange is rewritten.
@@ -602,7 +604,8 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         __syncwarp();
         asm volatile("bar.sync 2, 256;" ::: "memory");
         pend_mt = k.mt, pend_nt = k.nt, pend_piece = 0, pend_amax = 0.f;
-      } else if (ok && k.tl >= 0) {
+      } else if (k.tl >= 0) {
+        if (!ok) continue;
         // a slice of a split tail tile: its partial tile, token-major, rows contiguous
         float* so = P.tail + ((int64_t)k.ks * (P.tiles - P.whole) + k.tl) * TM * TN;
 #pragma unroll
@@ -610,7 +613,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
           const int t = t0 + c0 + i;
           so[(int64_t)(c0 + i) * TM + r] = t < P.m ? acc[i] * P.tscale[t] : 0.f;
         }
-      } else if (ok) {
+      } else if (!GATEUP && ok) {
         const int row = k.mt * TM + r;
         float* yo = P.y + (int64_t)k.ks * P.m * P.ldo;
 #pragma unroll
@@ -660,6 +663,63 @@ __global__ void __launch_bounds__(TM) finish_tail_kernel(const float* __restrict
     const int t = nt * TN + t8 * 8 + i;
     if (t < m) y[(int64_t)t * ldo + mt * TM + r] = v[i];
   }
+}
+
+// The split tail tiles of the gate/up projection: g and u = the sums of the tail_q partial
+// tiles in slice order (already scaled by 2^e_t), then h = silu(g) * u and its Q8_1, the rule
+// of the unsplit epilogue. One CTA of 256 threads per tail tile; thread e owns token e % 128
+// and the Q8_1 block e / 128 of the tile's 64 inter rows.
+__global__ void __launch_bounds__(256) finish_gateup_tail_kernel(const float* __restrict__ tail, int whole, int tiles,
+                                                                 int tail_q, int ntn, int mt_fast, int m, int ldo,
+                                                                 int8_t* __restrict__ hq_qs, float2* __restrict__ hq_ds) {
+  pdl_wait();
+  const int ntail = tiles - whole, tl = blockIdx.x;
+  const int tile = whole + tl, nmt = tiles / ntn;
+  const int nt = mt_fast ? tile / nmt : tile % ntn, mt = mt_fast ? tile % nmt : tile / ntn;
+  const int e = threadIdx.x, tt = e & (TN - 1), qb = e / TN;
+  const int t = nt * TN + tt;
+  if (t >= m) return;
+  float h[Q8B], amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < Q8B; j += 4) {
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int q = 0; q < tail_q; ++q) {
+      const float* pt = tail + (((int64_t)q * ntail + tl) * TN + tt) * TM;
+      const float4 gq = *reinterpret_cast<const float4*>(pt + qb * 32 + j);
+      const float4 uq = *reinterpret_cast<const float4*>(pt + 64 + qb * 32 + j);
+      g.x += gq.x, g.y += gq.y, g.z += gq.z, g.w += gq.w;
+      u.x += uq.x, u.y += uq.y, u.z += uq.z, u.w += uq.w;
+    }
+    h[j] = silu_f(g.x) * u.x;
+    h[j + 1] = silu_f(g.y) * u.y;
+    h[j + 2] = silu_f(g.z) * u.z;
+    h[j + 3] = silu_f(g.w) * u.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(h[j + i]));
+  }
+  const bool nz = amax >= 0x1p-120f;  // below: zero block (127/amax would overflow)
+  const float dq = nz ? __fdiv_rn(amax, 127.f) : 0.f;
+  const float inv = nz ? __fdiv_rn(127.f, amax) : 0.f;
+  int sum = 0;
+  uint32_t pk[Q8B / 4];
+#pragma unroll
+  for (int w = 0; w < Q8B / 4; ++w) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float rq = roundf(__fmul_rn(h[4 * w + b], inv));
+      rq = fminf(fmaxf(rq, -127.f), 127.f);
+      const int qi = (int)rq;
+      sum += qi;
+      v |= ((uint32_t)qi & 0xFFu) << (8 * b);
+    }
+    pk[w] = v;
+  }
+  const int irow = mt * 64 + qb * 32;
+  uint4* dst = reinterpret_cast<uint4*>(hq_qs + (int64_t)t * ldo + irow);  // 32-byte aligned
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  hq_ds[(int64_t)t * (ldo / Q8B) + irow / Q8B] = make_float2(dq, __fmul_rn(dq, (float)sum));
 }
 
 // Split of the down projection's last, partial round of tiles over num_sms persistent
@@ -757,13 +817,19 @@ bool prefill_plan(int64_t m, int64_t hidden, int64_t inter, int num_sms, Prefill
   p->tail_whole = dtiles, p->tail_q = 0;
   if (p->ksplit == 1) tail_split(dtiles, num_sms, &p->tail_whole, &p->tail_q);
   p->off_tail = take(p->tail_q > 1 ? (size_t)(dtiles - p->tail_whole) * p->tail_q * TM * TN * 4 : 0);
+  // gate/up: 64 inter rows (of gate and of up) per tile; slices of at least two superblocks
+  const int gtiles = (int)((inter / 64) * ((m + TN - 1) / TN));
+  tail_split(gtiles, num_sms, &p->gu_whole, &p->gu_q);
+  p->gu_q = std::min<int64_t>(p->gu_q, hidden / QK / 2);
+  if (p->gu_q < 2) p->gu_whole = gtiles, p->gu_q = 0;
+  p->off_gtail = take(p->gu_q > 1 ? (size_t)(gtiles - p->gu_whole) * p->gu_q * TM * TN * 4 : 0);
   p->off_ypart = take((size_t)p->ksplit * m * hidden * 4);  // also the float32 y of a bf16-output call
   p->ws_bytes = o;
   return true;
 }
 
 int prefill_kernels(const PrefillPlan& p, int ybf16) {
-  return (p.hidden <= QE_MAX_K ? 4 : 5) + (p.tail_q > 1) + (p.ksplit > 1 || ybf16);
+  return (p.hidden <= QE_MAX_K ? 4 : 5) + (p.gu_q > 1) + (p.tail_q > 1) + (p.ksplit > 1 || ybf16);
 }
 
 cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const void* wg, const void* wu,
@@ -825,12 +891,21 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.ksplit = 1;
   g.mt_fast = row_tiles_fastest(I / 64, ntn, H, p.num_sms);
   g.tiles = g.nwork = (int)(I / 64) * ntn;
+  g.whole = p.gu_whole;
+  g.tail_q = p.gu_q;
+  g.tail = (float*)(W + p.off_gtail);
+  if (p.gu_q > 1) g.nwork = p.gu_whole + (g.tiles - p.gu_whole) * p.gu_q;
   g.tscale = xo.scale;
   g.hq_qs = hq;
   g.hq_ds = hds;
   g.err = err;
   prof.before(1, s);
   e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s);
+  if (e == cudaSuccess && p.gu_q > 1) {  // the split tail tiles' sum, SwiGLU and Q8_1
+    finish_gateup_tail_kernel<<<g.tiles - p.gu_whole, 256, 0, s>>>(g.tail, p.gu_whole, g.tiles, p.gu_q, ntn,
+                                                                   g.mt_fast, (int)m, (int)I, hq, hds);
+    e = cudaGetLastError();
+  }
   prof.after(1, s);
   if (e != cudaSuccess) return e;
 

@@ -112,10 +112,26 @@ void check_prefill(int sms) {
           CHECK(al(p.off_tail) && p.off_tail + (size_t)ntail * p.tail_q * 128 * 128 * 4 <= p.ws_bytes,
                 "m %d h %d: tail scratch", m, h);
         }
+        const int gtiles = (i / 64) * ((m + 127) / 128);
+        CHECK(p.gu_q == 0 || (p.gu_q >= 2 && p.gu_q <= 8 && h / 256 / p.gu_q >= 2), "m %d h %d gu_q %d", m, h,
+              p.gu_q);
+        if (p.gu_q > 1) {
+          const int ntail = gtiles - p.gu_whole;
+          CHECK(p.gu_whole > 0 && p.gu_whole % sms == 0 && ntail > 0 && ntail * p.gu_q <= sms,
+                "m %d i %d: gate/up tail split %d %d", m, i, p.gu_whole, p.gu_q);
+          CHECK(al(p.off_gtail) && p.off_gtail + (size_t)ntail * p.gu_q * 128 * 128 * 4 <= p.ws_bytes,
+                "m %d i %d: gate/up tail scratch", m, i);
+        }
         const size_t offs[] = {p.off_xq, p.off_hq, p.off_xop, p.off_hop, p.off_misc, p.off_ypart};
         for (int k = 0; k < 6; ++k) CHECK(al(offs[k]) && offs[k] < p.ws_bytes, "m %d offset %d", m, k);
         CHECK(p.off_ypart + (size_t)p.ksplit * m * h * 4 <= p.ws_bytes, "m %d h %d partial outputs", m, h);
       }
+  // the LLaMA-7B FFN at 64 tokens: 172 gate/up tiles on 152 SMs, the last 20 split in 7
+  {
+    q4k::PrefillPlan p7;
+    CHECK(q4k::prefill_plan(64, 4096, 11008, 152, &p7) && p7.gu_whole == 152 && p7.gu_q == 7,
+          "7B gate/up tail split %d %d", p7.gu_whole, p7.gu_q);
+  }
   // the 27B-shaped long prefill: 640 down tiles on 152 SMs, the last 32 split in 4
   q4k::PrefillPlan p;
   CHECK(q4k::prefill_plan(2048, 5120, 17408, 152, &p) && p.ksplit == 1 && p.tail_whole == 608 && p.tail_q == 4,

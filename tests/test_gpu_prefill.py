@@ -108,3 +108,13 @@ def test_prefill_widest_hidden_sizes(H):
     c = workloads.small_config(H, 256, 25, "bf16", ("channels", 0.01, 100.0))
     y, ref, hq, wd = _run(c)
     _check(y, ref, hq, wd)
+
+
+@pytest.mark.parametrize("H,I,m", [(2048, 10240, 32), (1024, 10240, 200)])
+def test_prefill_gate_up_tail_split(H, I, m):
+    """More gate/up tiles than SMs with a short last round (160 and 320 tiles of 64 inter rows on
+    152 SMs): the last round's tiles are split along K, and their SwiGLU and Q8_1 follow the sum
+    of the slices in a separate kernel."""
+    c = workloads.small_config(H, I, m, "bf16", ("channels", 0.01, 100.0))
+    y, ref, hq, wd = _run(c)
+    _check(y, ref, hq, wd)
