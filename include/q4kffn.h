@@ -253,8 +253,8 @@ q4k_status q4k_test_bounded_wait(uint64_t limit_ns, q4k_stream_t stream);
  * GEMV, down chunk sum when K is split or y is bf16; a slot whose kernel does not
  * run records two adjacent events), prefill calls 4 (Q8_1 of x and its operand
  * expansion, gate+up MMQ + SwiGLU + Q8_1 of h, operand expansion of h, down MMQ;
- * the fourth slot also covers the split tiles' or K slices' sum when there is
- * one). Decode calls of
+ * the second and fourth slots also cover the sums of their split tiles or K
+ * slices when there are some). Decode calls of
  * 9..24 tokens record each pass's kernels into the same slots. Q6_K GEMV calls
  * record 2 (x fragments, GEMV). The events stay owned by the caller; n = 0 (events NULL) turns the
  * hook off. Recording between kernels serialises them, so timed runs of the
