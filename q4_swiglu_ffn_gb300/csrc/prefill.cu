@@ -316,7 +316,9 @@ __device__ __forceinline__ void gateup_final_piece(float* xg, const MmqParams& P
 // every pipeline (stages, TMEM buffers, their barrier phases) running on across
 // items, so one item's last superblocks and epilogue overlap the next item's first
 // loads and MMAs. SPLIT: the down projection at small m, K split into P.ksplit slices.
-template <bool GATEUP, bool SPLIT>
+// TAIL: the last round's tiles may be split along K (P.tail_q); gate/up builds without it
+// when there is no such round, so that its epilogue carries no partial-tile path.
+template <bool GATEUP, bool SPLIT, bool TAIL>
 __global__ void __launch_bounds__(NWARPS * 32, 1)
     mmq_kernel(const __grid_constant__ CUtensorMap tm_hi, const __grid_constant__ CUtensorMap tm_lo,
                const __grid_constant__ CUtensorMap tm_mn, const MmqParams P) {
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
     k.tl = -1;
     k.ks = SPLIT ? w / P.tiles : 0;
     int tile = w - k.ks * P.tiles;
-    if (!SPLIT && P.tail_q > 1 && w >= P.whole) {
+    if (TAIL && !SPLIT && P.tail_q > 1 && w >= P.whole) {
       const int j = w - P.whole, ntail = P.tiles - P.whole;
       k.tl = j % ntail;
       k.ks = j / ntail;
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       }
       if (!ok) *abort_flag = 1;
       const int t0 = k.nt * TN;
-      if (GATEUP && k.tl < 0) {
+      if (GATEUP && (!TAIL || k.tl < 0)) {
         // rows 0-63 hold gate, 64-127 up, for the same 64 inter indices. The previous
         // item's tail (steps left over when this item had fewer superblocks than steps)
         // finishes, and every warp is past it, before the exchange is rewritten.
@@ -604,7 +606,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         __syncwarp();
         asm volatile("bar.sync 2, 256;" ::: "memory");
         pend_mt = k.mt, pend_nt = k.nt, pend_piece = 0, pend_amax = 0.f;
-      } else if (k.tl >= 0) {
+      } else if (TAIL && k.tl >= 0) {
         if (!ok) continue;
         // a slice of a split tail tile: its partial tile, token-major, rows contiguous
         float* so = P.tail + ((int64_t)k.ks * (P.tiles - P.whole) + k.tl) * TM * TN;
@@ -740,11 +742,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
 }
 
 // One persistent CTA per SM (at most one per work item).
-template <bool GATEUP, bool SPLIT>
+template <bool GATEUP, bool SPLIT, bool TAIL>
 cudaError_t launch_mmq(const CUtensorMap& hi, const CUtensorMap& lo, const CUtensorMap& mn, const MmqParams& P,
                        int num_sms, cudaStream_t s) {
   const int grid = std::min(P.nwork, num_sms);
-  auto kern = mmq_kernel<GATEUP, SPLIT>;
+  auto kern = mmq_kernel<GATEUP, SPLIT, TAIL>;
   static uint64_t attr_set = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -900,7 +902,8 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   g.hq_ds = hds;
   g.err = err;
   prof.before(1, s);
-  e = launch_mmq<true, false>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s);
+  e = p.gu_q > 1 ? launch_mmq<true, false, true>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s)
+                 : launch_mmq<true, false, false>(mx_hi, mx_lo, mx_mn, g, p.num_sms, s);
   if (e == cudaSuccess && p.gu_q > 1) {  // the split tail tiles' sum, SwiGLU and Q8_1
     finish_gateup_tail_kernel<<<g.tiles - p.gu_whole, 256, 0, s>>>(g.tail, p.gu_whole, g.tiles, p.gu_q, ntn,
                                                                    g.mt_fast, (int)m, (int)I, hq, hds);
@@ -934,8 +937,8 @@ cudaError_t launch_prefill(const PrefillPlan& p, const void* x, int bf16, const 
   dn.y = fin ? ypart : (float*)y;
   dn.err = err;
   prof.before(3, s);  // the down MMQ, and the sum of its K slices when there are several
-  e = p.ksplit > 1 ? launch_mmq<false, true>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s)
-                   : launch_mmq<false, false>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s);
+  e = p.ksplit > 1 ? launch_mmq<false, true, false>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s)
+                   : launch_mmq<false, false, true>(mh_hi, mh_lo, mh_mn, dn, p.num_sms, s);
   if (e == cudaSuccess && p.tail_q > 1) {
     const int ntail = dn.tiles - p.tail_whole;
     finish_tail_kernel<<<ntail * (TN / 8), TM, 0, s>>>(dn.tail, p.tail_whole, dn.tiles, p.tail_q, ntn, dn.mt_fast,
