@@ -536,6 +536,23 @@ def gpu_int8_peak(world):
             "clocks": sampler.summary(t0, t1)}
 
 
+def gpu_tcgen05_issue():
+    """Cycles per tcgen05.mma kind::f16 (M 128, K 16) from one issuing thread per CTA at
+    N 128 and 256, and from two threads at N 128: the issue cost behind the prefill MMQ's
+    one N = 256 MMA per K step (the tensor pipe takes 4096 multiply-adds per cycle)."""
+    import q4_swiglu_ffn_gb300 as q
+    iters = 256 if QUICK else 2048
+    out = {}
+    for n, k in ((128, 1), (256, 1), (128, 2)):
+        q.q4k_bench_tcgen05_issue(n, k, 16)
+        c = q.q4k_bench_tcgen05_issue(n, k, iters)
+        out[f"n{n}_issuers{k}"] = {"cycles_per_mma": c, "pipe_fraction": k * 128 * n * 16 / c / 4096}
+    assert q.q4k_check_device_error() == 0
+    return {"per_issuing_thread": out,
+            "how": f"one CTA per SM, {iters} rounds of 4 MMAs per issuing thread, A in tensor memory, one commit "
+                   "per round; cycles of one issuing thread from its first MMA to its last MMA's completion"}
+
+
 def whole_job(ms_local: float, units_local: float, dist=None):
     """Max over ranks of the timed region (ms) and the whole-job rate: units summed
     over all ranks (each rank does the same work) divided by that time."""
@@ -677,6 +694,7 @@ def main():
         others["decode_tiny_h256_i768_m1"] = gpu_decode(workloads.TINY_DECODE, legK, 3, rank, 1, None)
         others["decode_13b_h5120_i13824_m8"] = gpu_decode(workloads.BATCHED_13B_DECODE, legK, 3, rank, 1, None)
     int8 = gpu_int8_peak(1) if (lead and not args.no_prefill) else None
+    tc_issue = gpu_tcgen05_issue() if (lead and not args.no_prefill) else None
     pre = {}
     if lead and not args.no_prefill:
         if not args.no_configs:
@@ -739,6 +757,8 @@ def main():
             "l2": f"rotating {r6['R']} weight replicas"}
     if int8 is not None:
         line["int8_tensor_peak"] = int8
+    if tc_issue is not None:
+        line["tcgen05_mma_issue"] = tc_issue
     for key, p in pre.items():
         line[key] = prefill_object(p, pk, pk_kind, int8)
     if f8 is not None:

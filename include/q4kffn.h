@@ -291,6 +291,18 @@ size_t q4k_mmq_fp8_workspace_bytes(int64_t m, int64_t k);
  * the caller. */
 q4k_status q4k_bench_int8_mma(int64_t iters, double* ops_per_launch, q4k_stream_t stream);
 
+/* Benchmark hook (no counterpart on the source pages): the issue rate of
+ * tcgen05.mma kind::f16 (M = 128, K = 16, N = n; A in tensor memory, fp32
+ * accumulators) when `issuers` threads per CTA issue back to back into their own
+ * accumulators, one CTA per SM, `iters` rounds of 4 MMAs per thread, one commit
+ * per round. Runs on `stream` and waits for it; *cycles_per_mma receives the SM
+ * cycles per MMA of one issuing thread (averaged over the CTAs): the tensor pipe's
+ * own rate is 4096 multiply-adds per cycle, 128 * n * 16 per MMA. n in {64, 128,
+ * 256}, issuers in {1, 2, 4}, n * issuers <= 256 and iters in 1..2^20, else
+ * Q4K_ERR_SHAPE; cycles_per_mma NULL gives Q4K_ERR_NULL. Its waits are bounded
+ * (q4k_check_device_error reports a timeout). Touches no memory of the caller. */
+q4k_status q4k_bench_tcgen05_issue(int n, int issuers, int64_t iters, double* cycles_per_mma, q4k_stream_t stream);
+
 /* Benchmark hook: how many kernels the most recent FFN or Q6_K GEMV call on
  * this thread launched (directly, or as nodes of the replayed graph). */
 int q4k_last_call_kernels(void);

@@ -51,6 +51,7 @@ _SIGS = {
     "q4k_last_call_kernels": (_int, []),
     "q4k_status_string": (ctypes.c_char_p, [_int]),
     "q4k_bench_int8_mma": (_int, [_i64, ctypes.POINTER(ctypes.c_double), _p]),
+    "q4k_bench_tcgen05_issue": (_int, [_int, _int, _i64, ctypes.POINTER(ctypes.c_double), _p]),
     "q4k_mmq_fp8": (_int, [_p, _i64, _i64, _p, _i64, _p, _p, _sz, _p]),
     "q4k_mmq_fp8_workspace_bytes": (_sz, [_i64, _i64]),
 }
@@ -293,6 +294,15 @@ def q4k_bench_int8_mma(iters: int, stream=None) -> float:
     ops = ctypes.c_double(0.0)
     _check(lib.q4k_bench_int8_mma(iters, ctypes.byref(ops), _stream(stream)), "q4k_bench_int8_mma")
     return ops.value
+
+
+def q4k_bench_tcgen05_issue(n: int, issuers: int, iters: int, stream=None) -> float:
+    """SM cycles per tcgen05.mma (M 128, N n, K 16) of one of `issuers` issuing threads per CTA
+    (benchmark hook; runs on the stream and waits for it)."""
+    cyc = ctypes.c_double(0.0)
+    _check(lib.q4k_bench_tcgen05_issue(n, issuers, iters, ctypes.byref(cyc), _stream(stream)),
+           "q4k_bench_tcgen05_issue")
+    return cyc.value
 
 
 def q4k_get_last_error() -> int:

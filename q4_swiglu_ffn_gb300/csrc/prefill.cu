@@ -28,10 +28,9 @@
 //                               (about 22 bits of v; e_t per token keeps |v| < 2^15).
 //                               The stage's hi tile and lo tile lie back to back, so
 //                               one N = 256 MMA takes both: D_main columns 0-127 get
-//                               A . hi, 128-255 A . lo. (One issuing thread keeps about
-//                               one MMA in flight, which takes about 123 cycles at
-//                               N = 128 and 137 at N = 256, so the wide one nearly
-//                               halves the time the MMAs take.)
+//                               A . hi, 128-255 A . lo: half the MMA instructions, and
+//                               half the predicate and descriptor work between them,
+//                               on the one issuing thread.
 // Each superblock (256 k) accumulates into D_main afresh; the epilogue warps add
 // d * (D_hi + D_lo) - 64*dmin * D_min into registers, where D_min is one
 // K = 16 MMA of the 6-bit mins against s8_j * 2^-(e_t+6) (hi and lo), s8_j =

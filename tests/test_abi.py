@@ -72,6 +72,15 @@ def test_argument_errors_before_any_launch(lib):
     w.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
     assert w(None, 0, 4, 256, A, None) == 1
     assert w(A, 0, 4, 255, A, None) == 2
+    b = lib.q4k_bench_tcgen05_issue
+    b.restype = ctypes.c_int
+    b.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p]
+    c = ctypes.c_double(0.0)
+    assert b(128, 1, 64, None, None) == 1                            # no result pointer
+    assert b(100, 1, 64, ctypes.byref(c), None) == 2                 # N not 64, 128 or 256
+    assert b(256, 2, 64, ctypes.byref(c), None) == 2                 # 512 accumulator columns
+    assert b(128, 3, 64, ctypes.byref(c), None) == 2                 # issuers not 1, 2 or 4
+    assert b(128, 1, 0, ctypes.byref(c), None) == 2                  # no rounds
 
 
 def test_status_strings(lib):

@@ -47,3 +47,4 @@ def test_context_usable_after_a_timeout():
     ref, _ = oracle.ffn_decode(x, wg, wu, wd)
     check_close(y.cpu().numpy(), ref, TIGHT_L2, TIGHT_MAX)
     assert q.q4k_check_device_error() == Q4K_OK
+
