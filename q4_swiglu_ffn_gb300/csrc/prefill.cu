@@ -504,10 +504,14 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             prefetch_row_l2(src + (int64_t)ahead * BLK);
           else if (ahead - k.nsbl < nsbl_n)
             prefetch_row_l2(src_n + (int64_t)(ahead - k.nsbl) * BLK);
+          // The superblock's 6-bit scales and mins, one byte each, four to a word: sub-blocks
+          // 0-3 are the low 6 bits of scale bytes 0-3 (4-7 for the mins); sub-blocks 4-7 take
+          // the low (high) nibbles of bytes 8-11 and, as bits 4-5, the top two bits of bytes
+          // 0-3 (4-7), the rule scale_min applies one value at a time.
           const uint4 hd = cur[0];
-          uint32_t scs[8], mns[8];  // all 6-bit scales and mins of this superblock
-#pragma unroll
-          for (int j = 0; j < 8; ++j) scale_min(hd.y, hd.z, hd.w, j, scs[j], mns[j]);
+          const uint32_t sc03 = hd.y & 0x3F3F3F3Fu, mn03 = hd.z & 0x3F3F3F3Fu;
+          const uint32_t sc47 = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+          const uint32_t mn47 = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
 #pragma unroll
           for (int c = 0; c < CH_PER_SB; ++c) {
             const int s = q % STAGES, u = q / STAGES;
@@ -520,10 +524,13 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             const uint32_t arow = a_lanes + s * A_COLS;
             if (c < 4) {
               uint32_t a[32];
-              unpack_chunk(cur[1 + 2 * c], cur[2 + 2 * c], scs[2 * c], scs[2 * c + 1], a);
+              const uint32_t sw = (c < 2 ? sc03 : sc47) >> (16 * (c & 1));  // sub-blocks 2c, 2c + 1
+              unpack_chunk(cur[1 + 2 * c], cur[2 + 2 * c], sw & 0xFFu, (sw >> 8) & 0xFFu, a);
               tmem_st32(arow, a);
             } else {
-              uint32_t v[8];
+              uint32_t mns[8], v[8];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) mns[j] = (mn03 >> (8 * j)) & 0xFFu, mns[4 + j] = (mn47 >> (8 * j)) & 0xFFu;
               min_operand(mns, v);
               tmem_st8(arow, v);
             }
