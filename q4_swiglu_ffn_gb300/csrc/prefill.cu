@@ -240,6 +240,9 @@ __device__ __forceinline__ void prefetch_row_l2(const uint8_t* p) {  // the <= 3
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p + BLK - 1));
 }
 
+constexpr int EPI_COLS = 8;  // accumulator columns an epilogue thread reads per TMEM load round
+static_assert(EPI_COLS == 8 || EPI_COLS == 16, "tmem_ld8 or tmem_ld16");
+
 constexpr uint32_t IDESC_MAIN = idesc_f16(TM, 2 * TN);  // B = the hi tile, then the lo tile
 constexpr uint32_t IDESC_MIN = idesc_f16(TM, TN);
 
@@ -579,20 +582,29 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
         if (!ok) continue;
         tc_fence_after();
         const uint32_t tm_hi = tmem + lane_addr + c0, tm_min = tmem + lane_addr + TM_DMIN + c0;
+        // EPI_COLS columns of each of D_hi, D_lo and D_min per round (fewer live registers
+        // than a wider round; the hand-over does not bind)
 #pragma unroll
-        for (int j = 0; j < TN / 32; ++j) {
-          float v[16], vl[16], u[16];
-          tmem_ld16(tm_hi + j * 16, v);
-          tmem_ld16(tm_hi + TN + j * 16, vl);
-          tmem_ld16(tm_min + j * 16, u);
+        for (int j = 0; j < TN / 2 / EPI_COLS; ++j) {
+          float v[EPI_COLS], vl[EPI_COLS], u[EPI_COLS];
+          if constexpr (EPI_COLS == 16) {
+            tmem_ld16(tm_hi + j * 16, v);
+            tmem_ld16(tm_hi + TN + j * 16, vl);
+            tmem_ld16(tm_min + j * 16, u);
+          } else {
+            tmem_ld8(tm_hi + j * 8, v);
+            tmem_ld8(tm_hi + TN + j * 8, vl);
+            tmem_ld8(tm_min + j * 8, u);
+          }
           tmem_wait_ld();
-          if (j == TN / 32 - 1) {  // every column of this warp is in registers: release the buffers
+          if (j == TN / 2 / EPI_COLS - 1) {  // every column of this warp is in registers: release the buffers
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce);
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(u[i], dmn, fmaf(v[i] + vl[i], d, acc[j * 16 + i]));
+          for (int i = 0; i < EPI_COLS; ++i)
+            acc[j * EPI_COLS + i] = fmaf(u[i], dmn, fmaf(v[i] + vl[i], d, acc[j * EPI_COLS + i]));
         }
         // one step of the previous item's tail while the MMAs run this item's next superblock
         if (GATEUP && pend_piece < FINAL_PIECES) final_step();
