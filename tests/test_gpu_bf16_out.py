@@ -1,5 +1,6 @@
 """The bf16-output entry point: every output is the float32 result rounded once to bf16
-(round to nearest even), on every path (decode, decode passes, prefill with and without K slices)."""
+(round to nearest even), on every path (decode, decode passes, prefill with and without K slices,
+and with the gate/up projection's last round split along K)."""
 import numpy as np
 import pytest
 
@@ -10,7 +11,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("H,I,m,xdt", [(1024, 2816, 1, "f32"), (512, 1536, 8, "bf16"), (1024, 768, 16, "f32"),
-                                        (512, 768, 48, "bf16"), (2304, 1280, 300, "bf16"), (4096, 2048, 64, "bf16")])
+                                        (512, 768, 48, "bf16"), (2304, 1280, 300, "bf16"), (4096, 2048, 64, "bf16"),
+                                        (2048, 10240, 32, "bf16")])
 def test_bf16_output_is_the_rounded_float32_output(H, I, m, xdt):
     c = workloads.small_config(H, I, m, xdt, ("channels", 0.01, 50.0))
     wg, wu, wd = [to_dev(a) for a in workloads.weights(c)]
