@@ -478,9 +478,12 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       };
       int nsbl_n;
       const uint8_t* src_n = next_row(w, nsbl_n);
-      uint4 raw[9];
+      // The current superblock's 144 bytes. Each chunk's 32 quant bytes are replaced by the next
+      // superblock's as soon as they are unpacked, and the header at the superblock's end, so
+      // every load has a superblock's time to land and no second copy is held.
+      uint4 cur[9];
 #pragma unroll
-      for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      for (int i = 0; i < 9; ++i) cur[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
 #pragma unroll
       for (int a = 1; a < PF_SB; ++a)
         if (a < k.nsbl) prefetch_row_l2(src + (int64_t)a * BLK);
@@ -488,20 +491,15 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
       bool ok = true;
       while (ok) {
         for (int sb = 0; sb < k.nsbl && ok; ++sb) {
-          uint4 cur[9];
-#pragma unroll
-          for (int i = 0; i < 9; ++i) cur[i] = raw[i];
-          // prefetch the next superblock: of this item, else the first of the next
+          // the next superblock: of this item, else the first of the next
           const uint8_t* nxt = nullptr;
           if (sb + 1 < k.nsbl)
             nxt = src + (int64_t)(sb + 1) * BLK;
           else if (w + (int)gridDim.x < P.nwork)
             nxt = row_ptr(work(w + gridDim.x), r);
-          if (nxt) {
-#pragma unroll
-            for (int i = 0; i < 9; ++i) raw[i] = __ldg(reinterpret_cast<const uint4*>(nxt) + i);
-          }
-          // and the superblock PF_SB ahead into L2, so that the load above finds it there
+          const uint4* nx4 = reinterpret_cast<const uint4*>(nxt);
+          const uint4 hd_n = nxt ? __ldg(nx4) : make_uint4(0, 0, 0, 0);
+          // and the superblock PF_SB ahead into L2, so that the loads of the next one find it there
           const int ahead = sb + PF_SB;
           if (ahead < k.nsbl)
             prefetch_row_l2(src + (int64_t)ahead * BLK);
@@ -529,6 +527,10 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
               uint32_t a[32];
               const uint32_t sw = (c < 2 ? sc03 : sc47) >> (16 * (c & 1));  // sub-blocks 2c, 2c + 1
               unpack_chunk(cur[1 + 2 * c], cur[2 + 2 * c], sw & 0xFFu, (sw >> 8) & 0xFFu, a);
+              if (nxt) {  // this chunk's quants of the next superblock, into the registers just read
+                cur[1 + 2 * c] = __ldg(nx4 + 1 + 2 * c);
+                cur[2 + 2 * c] = __ldg(nx4 + 2 + 2 * c);
+              }
               tmem_st32(arow, a);
             } else {
               uint32_t mns[8], v[8];
@@ -542,6 +544,7 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&full[s]);
           }
+          cur[0] = hd_n;
         }
         w += gridDim.x;
         if (w >= P.nwork) break;
