@@ -524,14 +524,16 @@ __global__ void __launch_bounds__(NWARPS * 32, 1)
             tc_fence_after();  // the MMAs that read this stage have completed
             const uint32_t arow = a_lanes + s * A_COLS;
             if (c < 4) {
-              uint32_t a[32];
               const uint32_t sw = (c < 2 ? sc03 : sc47) >> (16 * (c & 1));  // sub-blocks 2c, 2c + 1
-              unpack_chunk(cur[1 + 2 * c], cur[2 + 2 * c], sw & 0xFFu, (sw >> 8) & 0xFFu, a);
+              uint32_t a[16];  // the chunk's two sub-blocks in turn, 16 columns each
+              unpack_half<false>(cur[1 + 2 * c], cur[2 + 2 * c], sw & 0xFFu, a);
+              tmem_st16(arow, a);
+              unpack_half<true>(cur[1 + 2 * c], cur[2 + 2 * c], (sw >> 8) & 0xFFu, a);
               if (nxt) {  // this chunk's quants of the next superblock, into the registers just read
                 cur[1 + 2 * c] = __ldg(nx4 + 1 + 2 * c);
                 cur[2 + 2 * c] = __ldg(nx4 + 2 + 2 * c);
               }
-              tmem_st32(arow, a);
+              tmem_st16(arow + 16, a);
             } else {
               uint32_t mns[8], v[8];
 #pragma unroll

@@ -59,17 +59,7 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float v[8]) {
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-// Each lane stores 32 (8) consecutive 32-bit columns of its own TMEM lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
+// Each lane stores 8 consecutive 32-bit columns of its own TMEM lane (16 with tmem_st16 below).
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
@@ -100,28 +90,36 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   }
 }
 
-// One 64-k chunk of a Q4_K row as 32 fp16x2 columns (k = 2j, 2j + 1 in column j:
-// 32 low-nibble k of sub-block 2c, then 32 high-nibble k of sub-block 2c + 1).
-// ga, gb: the chunk's 32 quant bytes; sl, sh: the two sub-blocks' 6-bit scales.
-// Each quant becomes q * scale exactly: the 0x6400-exponent trick gives 1024 + q
-// (or 1024 + 16 q) and one fp16 fma scales it and removes the offset.
-__device__ __forceinline__ void unpack_chunk(uint4 ga, uint4 gb, uint32_t sl, uint32_t sh, uint32_t (&a)[32]) {
-  const __half2 mlo = __float2half2_rn((float)sl), alo = __float2half2_rn(-1024.f * (float)sl);
-  const __half2 mhi = __float2half2_rn((float)sh * 0.0625f), ahi = __float2half2_rn(-64.f * (float)sh);
+// One 64-k chunk of a Q4_K row is 32 fp16x2 TMEM columns (k = 2j, 2j + 1 in column j): 32
+// low-nibble k of sub-block 2c in columns 0-15, then 32 high-nibble k of sub-block 2c + 1 in
+// columns 16-31. unpack_half<false> gives the first 16 columns, unpack_half<true> the other
+// 16, so that a chunk is stored in two halves with half the registers live. ga, gb: the
+// chunk's 32 quant bytes; sc: the sub-block's 6-bit scale. Each quant becomes q * scale
+// exactly: the 0x6400-exponent trick gives 1024 + q (or 1024 + 16 q) and one fp16 fma scales
+// it and removes the offset; the multipliers come straight from the integer (exact in fp16).
+template <bool HI>
+__device__ __forceinline__ void unpack_half(uint4 ga, uint4 gb, uint32_t sc, uint32_t (&a)[16]) {
+  const __half hs = __uint2half_rn(sc);
+  const __half2 m = __half2half2(HI ? __hmul(hs, __float2half(0.0625f)) : hs);
+  const __half2 o = __half2half2(__hmul(hs, __float2half(HI ? -64.f : -1024.f)));
+  const uint32_t mask = HI ? 0x00F000F0u : 0x000F000Fu;
   const uint32_t wds[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     const uint32_t w0 = wds[2 * p], w1 = wds[2 * p + 1];
-    const uint32_t t0 = w0 >> 8, t1 = w1 >> 8;
-    a[4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-    a[4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x000F000Fu, 0x64006400u)), mlo, alo));
-    a[4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-    a[4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x000F000Fu, 0x64006400u)), mlo, alo));
-    a[16 + 4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-    a[16 + 4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t0, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-    a[16 + 4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
-    a[16 + 4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(t1, 0x00F000F0u, 0x64006400u)), mhi, ahi));
+    a[4 * p + 0] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0, mask, 0x64006400u)), m, o));
+    a[4 * p + 1] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w0 >> 8, mask, 0x64006400u)), m, o));
+    a[4 * p + 2] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1, mask, 0x64006400u)), m, o));
+    a[4 * p + 3] = h2_as_u32(__hfma2(u32_as_h2(lop3_and_or(w1 >> 8, mask, 0x64006400u)), m, o));
   }
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
 
 // The 8 mins of a superblock as A of the K = 16 min MMA: twice (k 0-7 against the
