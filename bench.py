@@ -538,12 +538,13 @@ def gpu_int8_peak(world):
 
 def gpu_tcgen05_issue():
     """Cycles per tcgen05.mma kind::f16 (M 128, K 16) from one issuing thread per CTA at
-    N 128 and 256, and from two threads at N 128: the issue cost behind the prefill MMQ's
-    one N = 256 MMA per K step (the tensor pipe takes 4096 multiply-adds per cycle)."""
+    N 64, 128 and 256, and from two threads at N 64 and 128: the issue cost behind the prefill
+    MMQ's one N = 256 MMA per K step (the tensor pipe takes 4096 multiply-adds per cycle), and
+    the floor of about 64 cycles per MMA of one issuing thread that narrow N does not lower."""
     import q4_swiglu_ffn_gb300 as q
     iters = 256 if QUICK else 2048
     out = {}
-    for n, k in ((128, 1), (256, 1), (128, 2)):
+    for n, k in ((64, 1), (128, 1), (256, 1), (64, 2), (128, 2)):
         q.q4k_bench_tcgen05_issue(n, k, 16)
         c = q.q4k_bench_tcgen05_issue(n, k, iters)
         out[f"n{n}_issuers{k}"] = {"cycles_per_mma": c, "pipe_fraction": k * 128 * n * 16 / c / 4096}
